@@ -1,0 +1,452 @@
+#!/usr/bin/env python
+"""Causal prefill attention throughput on GB300.
+
+One step = one causal forward pass (all of: K/V streaming, S = QK^T, online
+softmax, P V, epilogue) over the synthetic workload, inputs resident in HBM.
+The metric is causal TFLOP/s, counting 2*B*H*(S^2/2)*(d_qk+d_v) FLOPs, and
+its fraction of the GB300 dense tensor peak of the input type.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs the same workload on its own GPU (independent
+problems, no collective on the data path: weak scaling); rank 0 prints one
+JSON line.  ``--impl reference`` times the float64 CPU oracle on a bounded
+sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "causal fwd TFLOP/s and % of GB300 dense BF16/FP8 tensor peak, 1 GPU"
+DEFAULT_WORKLOAD = "bf16_gqa_b1_h32kv8_s16384_d128"
+ALSO_WORKLOADS = ["fp8_gqa_b1_h32kv8_s16384_d128"]
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCES = ["causal_flashattention_prefill_gb300/csrc/fwd_sm103.cu",
+                  "causal_flashattention_prefill_gb300/csrc/zyfa_ptx.cuh"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def tensor_peak(dtype: str, peaks: dict) -> float:
+    """Dense peak in TFLOP/s for the input type: BF16 measured burst; FP8 =
+    BF16 x 2 (the nominal dense ratio, 4.5 / 2.25 PFLOP/s)."""
+    bf16 = float(peaks["bf16_tflops"])
+    return bf16 if dtype == "bf16" else 2.0 * bf16
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        t = json.load(f)
+    e = t.get(workload)
+    if not e or e.get("kernel_hash") != kernel_hash():
+        return None
+    return float(e["bytes_per_launch"])
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock and throttle samples taken during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"zyfa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(parts[1]), max=float(parts[2]),
+                                     power=float(parts[3]), hw=parts[5], hwt=parts[6],
+                                     swt=parts[7], pcap=parts[8]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        loaded = [r for r in rows if r["power"] > 300.0] or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+                "sm_max_mhz": max(r["max"] for r in rows),
+                "power_w_max": max(r["power"] for r in rows),
+                "samples": len(rows), "samples_under_load": len(loaded),
+                "reasons": sorted(reasons)}
+
+
+# -------------------------------------------------------------- GPU timing
+
+def time_kernel(w, steps, warmup, device):
+    """Per-launch device time (CUDA events on the launching stream) with the
+    L2 flushed between launches; returns (ms list, result tensors)."""
+    import torch
+    import causal_flashattention_prefill_gb300 as zf
+
+    t = workloads.make_inputs(w)
+    q, k, v = (t[n].to(device) for n in ("q", "k", "v"))
+    ds = [None] * 3
+    if w.dtype == "fp8":
+        ds = [torch.tensor([t[n + "_descale"]], dtype=torch.float32, device=device)
+              for n in ("q", "k", "v")]
+    out_shape = (w.B, w.S, w.H, w.d_v) if w.layout == "bshd" else (w.B, w.H, w.S, w.d_v)
+    out = torch.empty(out_shape, dtype=torch.bfloat16, device=device)
+    lse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def launch():
+        zf.attention(q, k, v, out=out, lse=lse, q_descale=ds[0], k_descale=ds[1],
+                     v_descale=ds[2], layout=w.layout, return_lse=True,
+                     stream=stream.cuda_stream)
+
+    for _ in range(warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize(device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    return t, (q, k, v, ds, out, lse), launch, flush, starts, ends
+
+
+def run_timed(launch, flush, starts, ends, device):
+    import torch
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for s, e in zip(starts, ends):
+        flush.zero_()
+        s.record()
+        launch()
+        e.record()
+    torch.cuda.synchronize(device)
+    wall = time.perf_counter() - t0
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)], wall
+
+
+def sampled_parity(w, t, out, lse, n_rows=64):
+    """Checks a few rows of the timed launch against the oracle before timing."""
+    import oracle
+    rows = np.unique(np.concatenate([np.arange(4), np.array([w.S // 2, w.S - 1]),
+                                     np.random.default_rng(5).integers(0, w.S, n_rows)]))
+    heads = [0, w.H - 1]
+    q, k, v = (workloads.codes(t[n]) for n in ("q", "k", "v"))
+    worst = 0.0
+    worst_lse = 0.0
+    group = w.H // w.Hkv
+    for h in heads:
+        hk = h // group
+        sl_q = (slice(None), slice(None), [h]) if w.layout == "bshd" else (slice(None), [h])
+        sl_k = (slice(None), slice(None), [hk]) if w.layout == "bshd" else (slice(None), [hk])
+        O, L = oracle.attention_rows_f64(q[sl_q], k[sl_k], v[sl_k], rows, dtype=w.dtype,
+                                         layout=w.layout, q_descale=t["q_descale"],
+                                         k_descale=t["k_descale"], v_descale=t["v_descale"])
+        o = out.float().cpu().numpy()
+        og = o[:, rows, h] if w.layout == "bshd" else o[:, h, rows]
+        worst = max(worst, float(np.abs(og - O[:, 0]).max()))
+        worst_lse = max(worst_lse, float(np.abs(lse[:, h, rows].cpu().numpy() - L[:, 0]).max()))
+    tol = (1e-2, 1e-3) if w.dtype == "bf16" else (4e-2, 5e-3)
+    return {"rows": int(len(rows)), "heads": heads, "max_abs_dO": worst,
+            "max_abs_dLSE": worst_lse, "ok": bool(worst <= tol[0] and worst_lse <= tol[1])}
+
+
+def e2e_measure(w, t, steps, device):
+    """Same metric through the public API with host buffers: every step copies
+    q, k, v (and descales) from pinned host memory, runs the pass, and reads
+    O and LSE back to pinned host memory."""
+    import torch
+    import causal_flashattention_prefill_gb300 as zf
+
+    hq, hk, hv = (t[n].pin_memory() for n in ("q", "k", "v"))
+    dq, dk, dv = (torch.empty_like(x, device=device) for x in (hq, hk, hv))
+    hds = dds = [None] * 3
+    if w.dtype == "fp8":
+        hds = [torch.tensor([t[n + "_descale"]], dtype=torch.float32).pin_memory()
+               for n in ("q", "k", "v")]
+        dds = [torch.empty(1, dtype=torch.float32, device=device) for _ in range(3)]
+    out_shape = (w.B, w.S, w.H, w.d_v) if w.layout == "bshd" else (w.B, w.H, w.S, w.d_v)
+    dout = torch.empty(out_shape, dtype=torch.bfloat16, device=device)
+    dlse = torch.empty((w.B, w.H, w.S), dtype=torch.float32, device=device)
+    hout = torch.empty(out_shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty((w.B, w.H, w.S), dtype=torch.float32).pin_memory()
+
+    def step():
+        for d, h in zip((dq, dk, dv), (hq, hk, hv)):
+            d.copy_(h, non_blocking=True)
+        if w.dtype == "fp8":
+            for d, h in zip(dds, hds):
+                d.copy_(h, non_blocking=True)
+        zf.attention(dq, dk, dv, out=dout, lse=dlse, q_descale=dds[0], k_descale=dds[1],
+                     v_descale=dds[2], layout=w.layout, return_lse=True)
+        hout.copy_(dout, non_blocking=True)
+        hlse.copy_(dlse, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(device)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize(device)
+    dt = (time.perf_counter() - t0) / steps
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    h2d += 12 if w.dtype == "fp8" else 0
+    d2h = hout.numel() * hout.element_size() + hlse.numel() * hlse.element_size()
+    return {"value": w.flops / dt / 1e12, "unit": "TFLOP/s", "ms_per_step": dt * 1e3,
+            "steps": steps, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w, budget_s: float = 15.0, t=None):
+    """Times the float64 oracle on a bounded sample of the workload: the last
+    rows of the sequence (the longest causal rows) of successive (b, h) slices,
+    growing the sample until about ``budget_s`` seconds of CPU work."""
+    import oracle
+    if t is None:
+        t = workloads.make_inputs(w)
+    q, k, v = (workloads.codes(t[n]) for n in ("q", "k", "v"))
+    group = w.H // w.Hkv
+    R = min(w.S, 256)
+    rows = np.arange(w.S - R, w.S)
+    flops_per_head = float(sum(2.0 * (i + 1) * (w.d_qk + w.d_v) for i in rows))
+    elapsed = 0.0
+    heads_done = 0
+    while elapsed < budget_s and heads_done < w.B * w.H:
+        b, h = divmod(heads_done, w.H)
+        hk = h // group
+        if w.layout == "bshd":
+            qs, ks, vs = q[b:b + 1, :, h:h + 1], k[b:b + 1, :, hk:hk + 1], v[b:b + 1, :, hk:hk + 1]
+        else:
+            qs, ks, vs = q[b:b + 1, h:h + 1], k[b:b + 1, hk:hk + 1], v[b:b + 1, hk:hk + 1]
+        t0 = time.perf_counter()
+        oracle.attention_rows_f64(qs, ks, vs, rows, dtype=w.dtype, layout=w.layout,
+                                  q_descale=t["q_descale"], k_descale=t["k_descale"],
+                                  v_descale=t["v_descale"])
+        elapsed += time.perf_counter() - t0
+        heads_done += 1
+    flops = flops_per_head * heads_done
+    cores = len(os.sched_getaffinity(0))
+    return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": cores,
+            "kind": "oracle", "seconds": elapsed,
+            "sample": f"rows {w.S - R}..{w.S - 1} of {heads_done} (batch, head) slices of "
+                      f"{w.name} (numpy float64, materialised masked scores, "
+                      f"{cores} host threads available to BLAS)"}
+
+
+# ------------------------------------------------------------------ main
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the e2e, FP8 and CPU-baseline legs")
+    args = ap.parse_args()
+    warmup = max(3, args.warmup)
+    world, rank, local = dist_setup()
+    w = workloads.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        per_step = []
+        t = workloads.make_inputs(w)
+        # each step is one bounded sample, sized so the whole run stays within
+        # a few minutes
+        budget = max(0.05, min(20.0, 150.0 / (args.steps + warmup)))
+        for _ in range(warmup):
+            oracle_sample(w, budget_s=budget, t=t)
+        for _ in range(args.steps):
+            per_step.append(oracle_sample(w, budget_s=budget, t=t))
+        value = statistics.mean(s["value"] for s in per_step)
+        cpu = dict(per_step[0])
+        cpu["value"] = value
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": warmup,
+                "ms_per_step": 1e3 * statistics.mean(s["seconds"] for s in per_step),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic",
+                "config": {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "Hkv": w.Hkv,
+                           "d_qk": w.d_qk, "d_v": w.d_v, "layout": w.layout,
+                           "sample": cpu["sample"]},
+                "cpu_baseline": cpu,
+                "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    import causal_flashattention_prefill_gb300 as zf
+    from causal_flashattention_prefill_gb300 import build as zbuild
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    zbuild.build()
+    zf.load()
+
+    peaks, peak_src = load_peaks()
+    t, bufs, launch, flush, starts, ends = time_kernel(w, args.steps, warmup, device)
+    parity = sampled_parity(w, t, bufs[4], bufs[5]) if rank == 0 else None
+
+    if world > 1:
+        dist.barrier()
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    gpu_index = int(visible[device.index]) if len(visible) > device.index and \
+        visible[device.index].strip().isdigit() else device.index
+    with ClockSampler(gpu_index) as clk:
+        ms, wall = run_timed(launch, flush, starts, ends, device)
+    if world > 1:
+        dist.barrier()
+    mean_ms = statistics.mean(ms)
+    if world > 1:
+        tt = torch.tensor([mean_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        mean_ms = float(tt.item())
+    value = world * w.flops / (mean_ms * 1e-3) / 1e12
+    per_gpu = w.flops / (mean_ms * 1e-3) / 1e12
+    peak = tensor_peak(w.dtype, peaks)
+    traffic = load_traffic(w.name)
+
+    st, status_word = zf.zyfa_device_status()
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        also = []
+        for name in ALSO_WORKLOADS:
+            w2 = workloads.WORKLOADS[name]
+            t2, b2, l2, f2, s2, e2 = time_kernel(w2, max(20, args.steps // 5), warmup, device)
+            par2 = sampled_parity(w2, t2, b2[4], b2[5])
+            ms2, _ = run_timed(l2, f2, s2, e2, device)
+            v2 = w2.flops / (statistics.mean(ms2) * 1e-3) / 1e12
+            p2 = tensor_peak(w2.dtype, peaks)
+            also.append({"workload": name, "dtype": w2.dtype, "value": v2, "unit": "TFLOP/s",
+                         "ms_per_launch": statistics.mean(ms2), "peak": p2,
+                         "frac": v2 / p2, "parity": par2})
+            del t2, b2
+        extras["also"] = also
+        extras["e2e"] = e2e_measure(w, t, max(5, min(50, args.steps // 10)), device)
+        if world == 1:
+            extras["cpu_baseline"] = oracle_sample(w, budget_s=15.0, t=t)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": warmup, "ms_per_step": mean_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "S": w.S, "H": w.H, "Hkv": w.Hkv,
+                       "d_qk": w.d_qk, "d_v": w.d_v, "layout": w.layout,
+                       "values": "N(0,1) q, k, v" if w.values == "gaussian" else w.values,
+                       "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, "
+                             "outside the timed events)",
+                       "pct_of_peak": 100.0 * per_gpu / peak,
+                       "timed_wall_s": wall},
+            "roofline": {"bound": "tensor", "achieved": per_gpu, "peak": peak,
+                         "unit": "TFLOP/s", "frac": per_gpu / peak, "traffic": traffic,
+                         "peak_source": f"{peak_src} bf16 burst"
+                                        + (" x 2 (nominal FP8/BF16 ratio)" if w.dtype != "bf16"
+                                           else "")},
+            "gpu_launches": args.steps,
+            "parity_sample": parity,
+            "device_status_word": status_word,
+            "clocks": clk.summary(),
+            "kernel_hash": kernel_hash(),
+        }
+        if "e2e" in extras:
+            line["e2e"] = extras["e2e"]
+        if "cpu_baseline" in extras:
+            line["cpu_baseline"] = extras["cpu_baseline"]
+        if "also" in extras:
+            line["also"] = extras["also"]
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

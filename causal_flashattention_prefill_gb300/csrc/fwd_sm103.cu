@@ -1,0 +1,647 @@
+// Causal prefill attention forward for sm_103a (GB300).
+//
+// Computes O = softmax(scale * Q K^T + causal mask) V and the natural-log
+// LSE of each row of scaled scores, the operation the ZYFA README defines
+// ("Usage", "Supported configurations": causal forward pass, seqlen_q =
+// seqlen_k, MHA/GQA/MQA, d_qk = d_v = 128 or d_qk = 192 with d_v = 128,
+// BF16 or FP8 e4m3 inputs with one descale per tensor, BF16 output).
+//
+// One CTA per SM, persistent.  A work item is one query block of 256 rows
+// (two 128-row tiles, "stage 0" and "stage 1") of one (batch, head).  Both
+// tiles share every K/V tile that the CTA streams, so each K/V byte brought
+// on chip serves 256 query rows (the wider-query-tile idea of the CDNA4 post,
+// section 4.2, realised here as two tensor-memory accumulators).
+//
+// Warp roles (320 threads):
+//   warps 0-3  softmax of stage 0  (thread = query row = TMEM lane)
+//   warps 4-7  softmax of stage 1
+//   warp  8    TMA producer: Q tiles and a ring of K/V tile slots
+//   warp  9    MMA issuer: S = Q K^T (SS form) and O += P V (TS form, P read
+//              from tensor memory, V as an MN-major operand)
+//
+// Tensor memory (512 columns x 128 lanes of 32 bit):
+//   [0,128) S0   [128,256) S1   [256,384) O0   [384,512) O1
+// P of a stage is written over the first columns of that stage's S.
+//
+// Online softmax (FlashAttention-2 tiling; ZYFA README "Kernel design"):
+// exp2 with scale*log2(e) folded into one multiply-add, a reference maximum
+// per row that moves only when the row maximum exceeds it by more than tau
+// (lazy rescaling), and causal masking only on the diagonal tile.  Tiles
+// above the diagonal are never loaded or computed.  Keys and queries past the
+// end of the sequence read TMA's zero fill; the causal mask already hides
+// such keys from every real query, which is the exact equivalent of padding
+// the sequence with zeros (ZYFA README, "Usage").
+#include <cuda_bf16.h>
+
+#include "fwd.h"
+#include "zyfa_ptx.cuh"
+
+namespace zyfa {
+
+__device__ int g_zyfa_status;
+
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kBM = 128;  // query rows per stage
+constexpr int kBN = 128;  // keys per K/V tile
+constexpr int kDV = 128;
+constexpr int kMaxDynSmem = 232448;
+
+template <int DT, int DQK>
+struct Cfg {
+  static constexpr bool kF8 = DT == 1;
+  static constexpr int kElem = kF8 ? 1 : 2;
+  // Q and K: rows of DQK elements, stored as column chunks of one swizzle
+  // span each (128 bytes, or 64 bytes when the row is not a multiple of 128).
+  static constexpr int kRowBytesQK = DQK * kElem;
+  static constexpr int kSwzQK = (kRowBytesQK % 128 == 0) ? 128 : 64;
+  static constexpr uint32_t kSwzModeQK = kSwzQK == 128 ? 2u : 4u;
+  static constexpr int kChunkElemsQK = kSwzQK / kElem;
+  static constexpr int kChunksQK = kRowBytesQK / kSwzQK;
+  static constexpr int kChunkBytesQK = kBM * kSwzQK;
+  static constexpr int kTileBytesQK = kChunksQK * kChunkBytesQK;
+  // V: rows of 128 elements in 128-byte chunks.
+  static constexpr int kChunkElemsV = 128 / kElem;
+  static constexpr int kChunksV = kDV * kElem / 128;
+  static constexpr int kChunkBytesV = kBN * 128;
+  static constexpr int kTileBytesV = kChunksV * kChunkBytesV;
+  static constexpr int kSlotBytes = kTileBytesQK > kTileBytesV ? kTileBytesQK : kTileBytesV;
+  static constexpr int kUmmaK = 32 / kElem;   // reduction depth of one MMA
+  static constexpr int kReserve = 2048;       // alignment slack + barriers
+  static constexpr int kSlotsFit = (kMaxDynSmem - kReserve - 2 * kTileBytesQK) / kSlotBytes;
+  static constexpr int kNumSlots = kSlotsFit > 8 ? 8 : kSlotsFit;
+  static constexpr int kSmemBytes = kReserve + 2 * kTileBytesQK + kNumSlots * kSlotBytes;
+  // Lazy-rescale threshold in base-2 units of the score (ZYFA README,
+  // "Kernel design": 0.125 for FP8; BF16 keeps an FP32 accumulator with
+  // headroom, so it uses 8 as the CDNA4 post does).
+  static constexpr float kTau = kF8 ? 0.125f : 8.0f;
+  // FP8 P is stored as e4m3 of p * 2^8 (p <= 2^tau keeps it below 448); the
+  // factor enters as +8 in the exponent.
+  static constexpr float kPLog2Scale = kF8 ? 8.0f : 0.0f;
+  static constexpr uint32_t kFmt = kF8 ? 0u : 1u;   // E4M3 / BF16
+  static constexpr uint32_t kIdescQK = ptx::instr_desc(kFmt, kFmt, 0, kBM, kBN);
+  static constexpr uint32_t kIdescPV = ptx::instr_desc(kFmt, kFmt, 1, kBM, kDV);
+  static_assert(kNumSlots >= 2, "K/V ring needs at least two slots");
+  static_assert(kSmemBytes <= kMaxDynSmem, "shared memory budget");
+  static_assert(kSlotBytes % 1024 == 0 && kTileBytesQK % 1024 == 0, "1 KB alignment");
+};
+
+struct Item {
+  int b, h, u;
+  int n0, n1;     // K/V tiles processed by stage 0 and stage 1 (0 = stage idle)
+  int nload;      // K/V tiles loaded = max(n0, n1)
+};
+
+// Work items are ordered longest first: query block u descending, then batch,
+// then head (so the query heads of one KV group run side by side and share
+// K/V in L2).  CTA c of G takes, in round r, item r*G + c for even r and
+// r*G + G-1-c for odd r (a serpentine deal that evens out the decreasing
+// costs).  Stage 0 (tile 2u) needs K/V tiles 0..2u; stage 1 (tile 2u+1)
+// needs 0..2u+1 and is idle when all its rows lie past the sequence end.
+__device__ __forceinline__ int item_index(int round, int cta, int grid) {
+  return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
+}
+
+__device__ __forceinline__ Item decode_item(int w, const FwdParams& p) {
+  Item it;
+  const int per_block = p.B * p.H;
+  const int r = w / per_block;
+  const int rem = w - r * per_block;
+  it.u = p.n_qblocks - 1 - r;
+  it.b = rem / p.H;
+  it.h = rem - it.b * p.H;
+  it.n0 = 2 * it.u + 1;
+  it.n1 = (kBM * (2 * it.u + 1) < p.S) ? 2 * it.u + 2 : 0;
+  it.nload = it.n1 > it.n0 ? it.n1 : it.n0;
+  return it;
+}
+
+struct Smem {
+  uint8_t* q[2];
+  uint8_t* slots;
+  uint64_t* bars;
+  uint32_t* tmem_base;
+  int* abort;
+};
+
+// Barrier indices inside the barrier array.
+template <int NS>
+struct Bars {
+  static constexpr int kQFull = 0;            // [2]
+  static constexpr int kQEmpty = 2;           // [2]
+  static constexpr int kSFull = 4;            // [2]
+  static constexpr int kPFull = 6;            // [2]
+  static constexpr int kOFull = 8;            // [2]
+  static constexpr int kDrain = 10;
+  static constexpr int kPvDone = 11;          // [2]
+  static constexpr int kSlotFull = 13;        // [NS]
+  static constexpr int kSlotEmpty = 13 + NS;  // [NS]
+  static constexpr int kCount = 13 + 2 * NS;
+};
+
+__device__ __forceinline__ void tma_tile(const CUtensorMap* m, uint32_t dst, uint32_t bar,
+                                         int layout, int c0, int head, int row, int b,
+                                         uint64_t pol) {
+  if (layout == 0)
+    ptx::tma_load_4d(dst, m, bar, c0, head, row, b, pol);
+  else
+    ptx::tma_load_4d(dst, m, bar, c0, row, head, b, pol);
+}
+
+// One lane polls, the verdict is broadcast: the warp leaves the wait
+// converged and in agreement, as the .sync.aligned tcgen05 instructions that
+// follow require.
+__device__ __forceinline__ bool warp_wait(uint32_t b, uint32_t parity, volatile int* abort,
+                                          int* status, int lane) {
+  int ok = 0;
+  if (lane == 0) ok = ptx::mbar_wait(b, parity, abort, status, 1) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  // Each lane observes the completed phase itself (an acquire of its own);
+  // the phase cannot move on before this warp's next arrival.
+  if (ok) (void)ptx::mbar_try_wait(b, parity);
+  return ok != 0;
+}
+
+}  // namespace
+
+template <int DT, int DQK>
+__global__ void __launch_bounds__(kThreads, 1)
+    zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = Cfg<DT, DQK>;
+  constexpr int NS = C::kNumSlots;
+  using B = Bars<NS>;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  Smem sm;
+  sm.q[0] = base;
+  sm.q[1] = base + C::kTileBytesQK;
+  sm.slots = base + 2 * C::kTileBytesQK;
+  sm.bars = reinterpret_cast<uint64_t*>(sm.slots + NS * C::kSlotBytes);
+  sm.tmem_base = reinterpret_cast<uint32_t*>(sm.bars + B::kCount);
+  sm.abort = reinterpret_cast<int*>(sm.tmem_base + 1);
+  volatile int* abort = sm.abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return ptx::smem_u32(sm.bars + i); };
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(B::kQFull + 0), 1);
+    ptx::mbar_init(bar(B::kQFull + 1), 1);
+    ptx::mbar_init(bar(B::kQEmpty + 0), 1);
+    ptx::mbar_init(bar(B::kQEmpty + 1), 1);
+    ptx::mbar_init(bar(B::kSFull + 0), 1);
+    ptx::mbar_init(bar(B::kSFull + 1), 1);
+    ptx::mbar_init(bar(B::kPFull + 0), 4);
+    ptx::mbar_init(bar(B::kPFull + 1), 4);
+    ptx::mbar_init(bar(B::kOFull + 0), 1);
+    ptx::mbar_init(bar(B::kOFull + 1), 1);
+    ptx::mbar_init(bar(B::kDrain), 1);
+    ptx::mbar_init(bar(B::kPvDone + 0), 1);
+    ptx::mbar_init(bar(B::kPvDone + 1), 1);
+    for (int i = 0; i < NS; ++i) {
+      ptx::mbar_init(bar(B::kSlotFull + i), 1);
+      ptx::mbar_init(bar(B::kSlotEmpty + i), 1);
+    }
+    *sm.abort = 0;
+    ptx::fence_barrier_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    ptx::prefetch_tmap(&tm_q);
+    ptx::prefetch_tmap(&tm_k);
+    ptx::prefetch_tmap(&tm_v);
+  }
+  __syncwarp();
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_u32(sm.tmem_base), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *sm.tmem_base;
+
+  int* status = &g_zyfa_status;
+  const int grid = gridDim.x;
+  const int cta = blockIdx.x;
+
+  if (warp == kProducerWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_q = ptx::policy_evict_first();
+      const uint64_t pol_kv = ptx::policy_evict_last();
+      uint32_t q_uses[2] = {0, 0};
+      uint32_t t = 0;  // K/V tiles issued so far (ring position)
+      const int group = p.H / p.Hkv;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int w = item_index(r, cta, grid);
+        if (w >= p.total_items) break;
+        const Item it = decode_item(w, p);
+        for (int s = 0; s < 2 && ok; ++s) {
+          if (s == 1 && it.n1 == 0) break;
+          ok = ptx::mbar_wait(bar(B::kQEmpty + s), (q_uses[s] & 1u) ^ 1u, abort, status, 1);
+          if (!ok) break;
+          const uint32_t qb = bar(B::kQFull + s);
+          ptx::mbar_arrive_expect_tx(qb, C::kTileBytesQK);
+          const int row0 = (2 * it.u + s) * kBM;
+          for (int c = 0; c < C::kChunksQK; ++c)
+            tma_tile(&tm_q, ptx::smem_u32(sm.q[s] + c * C::kChunkBytesQK), qb, p.layout,
+                     c * C::kChunkElemsQK, it.h, row0, it.b, pol_q);
+          ++q_uses[s];
+        }
+        const int hk = it.h / group;
+        for (int j = 0; j < it.nload && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t slot = t % NS;
+            ok = ptx::mbar_wait(bar(B::kSlotEmpty + slot), ((t / NS) & 1u) ^ 1u, abort, status,
+                                1);
+            if (!ok) break;
+            const uint32_t fb = bar(B::kSlotFull + slot);
+            const uint32_t dst = ptx::smem_u32(sm.slots + slot * C::kSlotBytes);
+            if (kv == 0) {
+              ptx::mbar_arrive_expect_tx(fb, C::kTileBytesQK);
+              for (int c = 0; c < C::kChunksQK; ++c)
+                tma_tile(&tm_k, dst + c * C::kChunkBytesQK, fb, p.layout,
+                         c * C::kChunkElemsQK, hk, j * kBN, it.b, pol_kv);
+            } else {
+              ptx::mbar_arrive_expect_tx(fb, C::kTileBytesV);
+              for (int c = 0; c < C::kChunksV; ++c)
+                tma_tile(&tm_v, dst + c * C::kChunkBytesV, fb, p.layout, c * C::kChunkElemsV,
+                         hk, j * kBN, it.b, pol_kv);
+            }
+            ++t;
+          }
+        }
+      }
+      if (!ok) {
+        // Unwind: let every copy this thread issued land before the CTA's
+        // shared memory is released.
+        for (uint32_t i = 0; i < NS && i < t; ++i) {
+          const uint32_t last = t - 1 - i;  // the last use of slot last % NS
+          ptx::mbar_drain(bar(B::kSlotFull + last % NS), (last / NS) & 1u);
+        }
+        for (int s = 0; s < 2; ++s)
+          if (q_uses[s]) ptx::mbar_drain(bar(B::kQFull + s), (q_uses[s] - 1) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t q_uses[2] = {0, 0};
+      uint32_t p_uses[2] = {0, 0};
+      uint32_t pv_uses[2] = {0, 0};
+      uint32_t t = 0;
+      bool ok = true;
+      const uint32_t tm_s[2] = {tmem + 0, tmem + 128};
+      const uint32_t tm_o[2] = {tmem + 256, tmem + 384};
+      const uint32_t q_addr[2] = {ptx::smem_u32(sm.q[0]), ptx::smem_u32(sm.q[1])};
+      const uint32_t slots_addr = ptx::smem_u32(sm.slots);
+
+      auto issue_s = [&](int s, uint32_t slot) {
+        const uint32_t kaddr = slots_addr + slot * C::kSlotBytes;
+#pragma unroll
+        for (int c = 0; c < C::kChunksQK; ++c) {
+#pragma unroll
+          for (int kk = 0; kk < C::kSwzQK / 32; ++kk) {
+            const uint32_t off = c * C::kChunkBytesQK + kk * 32;
+            const uint64_t da = ptx::smem_desc(q_addr[s] + off, 16, 8 * C::kSwzQK, C::kSwzModeQK);
+            const uint64_t db = ptx::smem_desc(kaddr + off, 16, 8 * C::kSwzQK, C::kSwzModeQK);
+            ptx::mma_ss<C::kF8>(tm_s[s], da, db, C::kIdescQK, (c | kk) != 0);
+          }
+        }
+      };
+      // O_s (+)= P V_j, with P read from tensor memory at column offset
+      // p_col of S_s (FP8 keeps a second, residual P term at offset 32).
+      auto issue_pv = [&](int s, uint32_t slot, bool acc_first, uint32_t p_col) {
+        const uint32_t vaddr = slots_addr + slot * C::kSlotBytes;
+#pragma unroll
+        for (int ks = 0; ks < kBN / C::kUmmaK; ++ks) {
+          const uint64_t db =
+              ptx::smem_desc(vaddr + ks * C::kUmmaK * 128, C::kChunkBytesV, 1024, 2u);
+          ptx::mma_ts<C::kF8>(tm_o[s], tm_s[s] + p_col + ks * 8, db, C::kIdescPV,
+                              (acc_first || ks > 0) ? 1u : 0u);
+        }
+      };
+
+      for (int r = 0; ok; ++r) {
+        const int w = item_index(r, cta, grid);
+        if (w >= p.total_items) break;
+        const Item it = decode_item(w, p);
+        const int nst = it.n1 > 0 ? 2 : 1;
+        for (int s = 0; s < nst && ok; ++s) {
+          ok = ptx::mbar_wait(bar(B::kQFull + s), q_uses[s] & 1u, abort, status, 1);
+          ++q_uses[s];
+        }
+        if (!ok) break;
+        // Prologue: S of K/V tile 0 for both stages.
+        uint32_t slot_k = t % NS;
+        ok = ptx::mbar_wait(bar(B::kSlotFull + slot_k), (t / NS) & 1u, abort, status, 1);
+        if (!ok) break;
+        ++t;
+        ptx::tc_fence_after();
+        issue_s(0, slot_k);
+        ptx::mma_commit(bar(B::kSFull + 0));
+        if (it.n1 > 0) {
+          issue_s(1, slot_k);
+          ptx::mma_commit(bar(B::kSFull + 1));
+        }
+        ptx::mma_commit(bar(B::kSlotEmpty + slot_k));
+
+        for (int j = 0; j < it.nload && ok; ++j) {
+          const uint32_t slot_v = t % NS;
+          const uint32_t par_v = (t / NS) & 1u;
+          ++t;
+          const bool has_next = j + 1 < it.nload;
+          uint32_t par_k = 0;
+          if (has_next) {
+            slot_k = t % NS;
+            par_k = (t / NS) & 1u;
+            ++t;
+          }
+          bool k_ready = false;
+          ok = ptx::mbar_wait(bar(B::kSlotFull + slot_v), par_v, abort, status, 1);
+          if (!ok) break;
+          for (int s = 0; s < 2; ++s) {
+            const int ns = s == 0 ? it.n0 : it.n1;
+            if (j >= ns) continue;
+            ok = ptx::mbar_wait(bar(B::kPFull + s), p_uses[s] & 1u, abort, status, 1);
+            if (!ok) break;
+            ++p_uses[s];
+            ptx::tc_fence_after();
+            issue_pv(s, slot_v, j > 0, 0);
+            if (C::kF8 && j + 1 == ns) issue_pv(s, slot_v, true, 32);  // lo term of P
+            if (p.serialize_pv && j + 1 < ns) {
+              // Verification mode: P (aliasing S) is fully consumed before the
+              // next S MMA of this stage overwrites it.
+              ptx::mma_commit(bar(B::kPvDone + s));
+              ok = ptx::mbar_wait(bar(B::kPvDone + s), pv_uses[s] & 1u, abort, status, 1);
+              ++pv_uses[s];
+              if (!ok) break;
+            }
+            if (j + 1 < ns) {
+              if (!k_ready) {
+                ok = ptx::mbar_wait(bar(B::kSlotFull + slot_k), par_k, abort, status, 1);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                k_ready = true;
+              }
+              issue_s(s, slot_k);
+              ptx::mma_commit(bar(B::kSFull + s));
+            } else {
+              ptx::mma_commit(bar(B::kOFull + s));
+            }
+          }
+          if (!ok) break;
+          ptx::mma_commit(bar(B::kSlotEmpty + slot_v));
+          if (has_next) ptx::mma_commit(bar(B::kSlotEmpty + slot_k));
+        }
+        if (!ok) break;
+        for (int s = 0; s < nst; ++s) ptx::mma_commit(bar(B::kQEmpty + s));
+      }
+      // Every MMA this thread issued completes before tensor memory is freed.
+      ptx::mma_commit(bar(B::kDrain));
+      ptx::mbar_drain(bar(B::kDrain), 0);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int s = warp >> 2;            // stage
+    const int wq = warp & 3;            // lane quarter of TMEM this warp may access
+    const int row_in_tile = wq * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_base + (s ? 128u : 0u);
+    const uint32_t t_o = tmem + lane_base + (s ? 384u : 256u);
+    float c_log2 = p.softmax_scale * 1.4426950408889634f;
+    float o_extra = 1.0f;
+    if constexpr (C::kF8) {
+      c_log2 *= __ldg(p.q_descale) * __ldg(p.k_descale);
+      o_extra = __ldg(p.v_descale);
+    }
+    uint32_t s_uses = 0, o_uses = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int w = item_index(r, cta, grid);
+      if (w >= p.total_items) break;
+      const Item it = decode_item(w, p);
+      const int ns = s == 0 ? it.n0 : it.n1;
+      if (ns == 0) continue;
+      const int tile = 2 * it.u + s;
+      float m_ref = -INFINITY;  // reference maximum, base-2 units of the scaled score
+      float l = 0.f;            // sum of 2^(x - m_ref + kPLog2Scale), unrounded (for LSE)
+      float lr = 0.f;           // the same sum over the rounded (BF16 / e4m3) values that
+                                // multiply V: the denominator of O
+      for (int j = 0; j < ns; ++j) {
+        ok = warp_wait(bar(B::kSFull + s), s_uses & 1u, abort, status, lane);
+        if (!ok) break;
+        ++s_uses;
+        ptx::tc_fence_after();
+        uint32_t v[128];
+        ptx::tmem_ld128_wait(t_s, v);
+        float* f = reinterpret_cast<float*>(v);
+        if (j == tile) {
+          // Diagonal tile: key (row_in_tile + d) for d > 0 is in the future.
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > row_in_tile) f[c] = -INFINITY;
+        }
+        float mx = f[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, f[c]);
+        mx *= c_log2;
+        if (j == 0) {
+          m_ref = mx;
+        } else {
+          const bool need = mx > m_ref + C::kTau;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ptx::ex2(m_ref - mx) : 1.0f;
+            if (need) {
+              l *= alpha;
+              lr *= alpha;
+              m_ref = mx;
+            }
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[32];
+              ptx::tmem_ld32_wait(t_o + c * 32, o);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+              ptx::tmem_st32(t_o + c * 32, o);
+            }
+            ptx::tmem_wait_st();
+          }
+        }
+        const float neg_m = C::kPLog2Scale - m_ref;
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          const float e = ptx::ex2(fmaf(f[c], c_log2, neg_m));
+          rs += e;
+          f[c] = e;
+        }
+        l += rs;
+        if constexpr (C::kF8) {
+          uint32_t pk[32];
+          if (j != tile) {
+            uint32_t acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // FP16x2 partial sums of rounded P
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              pk[i] = ptx::pack_e4m3x4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+              ptx::add_e4m3x4_f16x2(pk[i], acc[2 * (i & 3)], acc[2 * (i & 3) + 1]);
+            }
+            ptx::tmem_st32(t_s, pk);
+            float rr = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) rr += ptx::f16x2_sum_f32(acc[i]);
+            lr += rr;
+          } else {
+            // Diagonal tile: its rows see few keys (row i of the first tile
+            // sees i + 1), so one e4m3 rounding of a probability shows in
+            // the output.  P is stored as two e4m3 terms, hi + lo, where lo
+            // is the rounding residual of hi; the MMA issuer adds a second
+            // P V product for lo, giving P about 8 significant bits here.
+            uint32_t lo[32];
+            float rr = 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              pk[i] = ptx::pack_e4m3x4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+              float d[4];
+              ptx::unpack_e4m3x4(pk[i], d);
+              lo[i] = ptx::pack_e4m3x4(f[4 * i] - d[0], f[4 * i + 1] - d[1],
+                                       f[4 * i + 2] - d[2], f[4 * i + 3] - d[3]);
+              float e[4];
+              ptx::unpack_e4m3x4(lo[i], e);
+              rr += (d[0] + e[0]) + (d[1] + e[1]) + (d[2] + e[2]) + (d[3] + e[3]);
+            }
+            ptx::tmem_st32(t_s, pk);
+            ptx::tmem_st32(t_s + 32, lo);
+            lr += rr;
+          }
+        } else {
+          // BF16: the denominator of O is the sum of the same rounded
+          // probabilities that multiply V, so the output weights sum to one
+          // (ZYFA README, "Accuracy"); a BF16 pair unpacks exactly by shifts.
+          float rr = 0.f;
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              pk[i] = ptx::pack_bf16x2(f[64 * h2 + 2 * i], f[64 * h2 + 2 * i + 1]);
+              rr += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+            }
+            ptx::tmem_st32(t_s + h2 * 32, pk);
+          }
+          lr += rr;
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(B::kPFull + s));
+      }
+      if (!ok) break;
+      // Epilogue: O / l (times v_descale and 2^-8 for FP8), BF16, and LSE.
+      ok = warp_wait(bar(B::kOFull + s), o_uses & 1u, abort, status, lane);
+      if (!ok) break;
+      ++o_uses;
+      ptx::tc_fence_after();
+      const int row = tile * kBM + row_in_tile;
+      const bool valid = row < p.S;
+      const float inv = o_extra / lr;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+      const int64_t orow =
+          p.layout == 0
+              ? ((static_cast<int64_t>(it.b) * p.S + row) * p.H + it.h) * kDV
+              : ((static_cast<int64_t>(it.b) * p.H + it.h) * p.S + row) * kDV;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        ptx::tmem_ld32_wait(t_o + c * 32, o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv,
+                                   __uint_as_float(o[2 * i + 1]) * inv);
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(out + orow + c * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+      }
+      if (valid && p.lse != nullptr) {
+        p.lse[(static_cast<int64_t>(it.b) * p.H + it.h) * p.S + row] =
+            (m_ref + log2f(l) - C::kPLog2Scale) * 0.6931471805599453f;
+      }
+      ptx::tc_fence_before();
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------- host side
+
+template <int DT, int DQK>
+static int launch_one(const FwdParams& p, const TensorMaps& m, int grid, cudaStream_t stream) {
+  using C = Cfg<DT, DQK>;
+  auto kern = zyfa_fwd_kernel<DT, DQK>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, C::kSmemBytes, stream>>>(m.q, m.k, m.v, p);
+  return cudaGetLastError();
+}
+
+int launch_fwd(int dtype, int d_qk, const FwdParams& p, const TensorMaps& maps, int grid,
+               cudaStream_t stream) {
+  if (dtype == 0 && d_qk == 128) return launch_one<0, 128>(p, maps, grid, stream);
+  if (dtype == 0 && d_qk == 192) return launch_one<0, 192>(p, maps, grid, stream);
+  if (dtype == 1 && d_qk == 128) return launch_one<1, 128>(p, maps, grid, stream);
+  if (dtype == 1 && d_qk == 192) return launch_one<1, 192>(p, maps, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+template <int DT, int DQK>
+static void geometry_of(KernelGeometry* g) {
+  using C = Cfg<DT, DQK>;
+  g->smem_bytes = C::kSmemBytes;
+  g->qk_box_elems = C::kChunkElemsQK;
+  g->qk_swizzle = C::kSwzQK;
+  g->v_box_elems = C::kChunkElemsV;
+  g->num_slots = C::kNumSlots;
+}
+
+int kernel_geometry(int dtype, int d_qk, KernelGeometry* g) {
+  if (dtype == 0 && d_qk == 128) return geometry_of<0, 128>(g), 0;
+  if (dtype == 0 && d_qk == 192) return geometry_of<0, 192>(g), 0;
+  if (dtype == 1 && d_qk == 128) return geometry_of<1, 128>(g), 0;
+  if (dtype == 1 && d_qk == 192) return geometry_of<1, 192>(g), 0;
+  return -1;
+}
+
+int read_device_status(int* value, int reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_zyfa_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  if (reset) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_zyfa_status, &zero, sizeof(int));
+  }
+  return e;
+}
+
+}  // namespace zyfa

@@ -1,0 +1,131 @@
+/*
+ * zyfa.h -- C ABI of the GB300 (sm_103a) causal prefill attention library.
+ *
+ * The operation is the causal forward attention pass for inference prefill
+ * that the ZYFA README defines ("Usage" and "Supported configurations"):
+ *
+ *   O[b, i, h, :] = sum_{j <= i} softmax_j(scale * <q[b,i,h], k[b,j,hk]>) v[b,j,hk]
+ *   LSE[b, h, i]  = ln sum_{j <= i} exp(scale * <q[b,i,h], k[b,j,hk]>)
+ *
+ * with seqlen_q = seqlen_k = S, equal-length batches, hk = h / (H / Hkv)
+ * (MHA, GQA and MQA: "nheads a multiple of nheads_k"), head dims
+ * d_qk = d_v = 128 or d_qk = 192 with d_v = 128, BF16 or FP8 e4m3 inputs with
+ * one descale per tensor (applied by the kernel from device memory; "Usage":
+ * "The kernel reads tensor descales from GPU memory and applies all three
+ * itself"), BF16 output and an optional FP32 natural-log LSE of the scaled
+ * scores.  Any S >= 1 is accepted: lengths that are not a multiple of the tile
+ * give the same result as zero-padding ("Usage": padding is exact for causal
+ * attention), with no copy.
+ *
+ * Layouts (all tensors dense and contiguous, element strides implied):
+ *   ZYFA_BSHD: q (B,S,H,d_qk)  k (B,S,Hkv,d_qk)  v (B,S,Hkv,d_v)  out (B,S,H,d_v)
+ *   ZYFA_BHSD: q (B,H,S,d_qk)  k (B,Hkv,S,d_qk)  v (B,Hkv,S,d_v)  out (B,H,S,d_v)
+ *   lse is (B,H,S) FP32 in both layouts.
+ *
+ * Ownership and synchronisation: every pointer is a device pointer owned by
+ * the caller.  The library allocates nothing per call (no workspace, no host
+ * job table) and never synchronises the host: a call only enqueues one kernel
+ * on `stream`, so it can be captured in a CUDA graph from the first call.
+ *
+ * Errors: argument checks run on the host before any CUDA call and return a
+ * negative zyfa_status without launching anything.  Launch failures return
+ * ZYFA_ERR_LAUNCH.  Asynchronous device errors surface on the caller's next
+ * synchronisation.  Every wait inside the kernel is bounded (2 s); a wait that
+ * runs out makes the kernel unwind and sets bit 0 of the device status word
+ * read by zyfa_device_status().
+ */
+#ifndef ZYFA_H
+#define ZYFA_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ZYFA_API __attribute__((visibility("default")))
+#else
+#define ZYFA_API
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st*`; NULL = default stream */
+
+typedef enum {
+  ZYFA_OK = 0,
+  ZYFA_ERR_ARG = -1,            /* invalid value (sizes, enums, NULL pointers)       */
+  ZYFA_ERR_UNSUPPORTED = -2,    /* valid request outside the supported configurations */
+  ZYFA_ERR_ALIGN = -3,          /* a pointer is not 16-byte aligned (lse: 4-byte)   */
+  ZYFA_ERR_LAUNCH = -4,         /* the kernel launch failed                          */
+  ZYFA_ERR_DEVICE = -5,         /* no usable sm_103 device / driver entry point      */
+  ZYFA_ERR_DEVICE_TIMEOUT = -6  /* reported by zyfa_device_status()                  */
+} zyfa_status;
+
+enum { ZYFA_BF16 = 0, ZYFA_FP8_E4M3 = 1 };
+enum { ZYFA_BSHD = 0, ZYFA_BHSD = 1 };
+
+/*
+ * Causal forward attention with softmax_scale = 1/sqrt(d_qk).
+ *
+ * q, k, v    device, BF16 (dtype ZYFA_BF16) or e4m3 codes (ZYFA_FP8_E4M3),
+ *            16-byte aligned, shapes per `layout` above.
+ * out        device, BF16, 16-byte aligned; written for every (b, i, h).
+ * lse        device FP32 (B,H,S), 4-byte aligned, or NULL to skip it.
+ * B, S       batch size >= 1 and sequence length >= 1 (queries = keys = S).
+ * H, Hkv     query heads and KV heads, H % Hkv == 0.
+ * d_qk, d_v  (128, 128) or (192, 128).
+ * q_descale, k_descale, v_descale
+ *            FP8: device pointers to one FP32 each (the factor that maps
+ *            the e4m3 tensor back to its range); the values must be positive
+ *            normal floats and are not checked.  BF16: ignored (may be NULL).
+ * layout     ZYFA_BSHD or ZYFA_BHSD.
+ * stream     CUDA stream the kernel is enqueued on.
+ * Returns ZYFA_OK or a negative zyfa_status.
+ */
+ZYFA_API int zyfa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int S,
+             int H, int Hkv, int d_qk, int d_v, int dtype, const float* q_descale,
+             const float* k_descale, const float* v_descale, int layout,
+             struct CUstream_st* stream);
+
+/* Same as zyfa_fwd with an explicit softmax_scale (finite, > 0). */
+ZYFA_API int zyfa_fwd_scaled(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                    int S, int H, int Hkv, int d_qk, int d_v, int dtype, const float* q_descale,
+                    const float* k_descale, const float* v_descale, float softmax_scale,
+                    int layout, struct CUstream_st* stream);
+
+/*
+ * Runs only the host-side argument checks of zyfa_fwd_scaled (no CUDA call).
+ * Returns ZYFA_OK when zyfa_fwd_scaled would launch.
+ */
+ZYFA_API int zyfa_validate(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                  int S, int H, int Hkv, int d_qk, int d_v, int dtype, const float* q_descale,
+                  const float* k_descale, const float* v_descale, float softmax_scale,
+                  int layout);
+
+/* Static description of a status code; never NULL. */
+ZYFA_API const char* zyfa_status_string(int status);
+
+/*
+ * Reads the device status word of the current device into *value (0 = no
+ * wait has timed out; bit 0 = a kernel wait timed out) and clears it when
+ * `reset` is non-zero.  Synchronous.  Returns ZYFA_OK or ZYFA_ERR_DEVICE.
+ */
+ZYFA_API int zyfa_device_status(int* value, int reset);
+
+/*
+ * Library options (process-wide; take effect on the next call).
+ *   ZYFA_OPT_SERIALIZE_PV: when 1, the kernel waits for each P*V product to
+ *   finish before the next score product of the same query tile overwrites
+ *   the tensor memory that holds P.  Results are identical; it exists to
+ *   verify that the default pipelined order is race-free.  Default 0.
+ * Returns ZYFA_OK or ZYFA_ERR_ARG.
+ */
+enum { ZYFA_OPT_SERIALIZE_PV = 1 };
+ZYFA_API int zyfa_set_option(int option, int value);
+
+/* ABI version, (major << 16) | minor. */
+ZYFA_API int zyfa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZYFA_H */
