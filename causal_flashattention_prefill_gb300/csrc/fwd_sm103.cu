@@ -12,12 +12,14 @@
 // on chip serves 256 query rows (the wider-query-tile idea of the CDNA4 post,
 // section 4.2, realised here as two tensor-memory accumulators).
 //
-// Warp roles (320 threads):
+// Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax of stage 0  (thread = query row = TMEM lane)
 //   warps 4-7  softmax of stage 1
 //   warp  8    TMA producer: Q tiles and a ring of K/V tile slots
 //   warp  9    MMA issuer: S = Q K^T (SS form) and O += P V (TS form, P read
 //              from tensor memory, V as an MN-major operand)
+//   warps 10-11 idle (they complete the third warpgroup so that registers
+//              can move to the softmax warpgroups with setmaxnreg)
 //
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   [0,128) S0   [128,256) S1   [256,384) O0   [384,512) O1
@@ -42,9 +44,14 @@ __device__ int g_zyfa_status;
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+// Register split (setmaxnreg): the launch gives 384 x 168 = 64512 registers;
+// the two softmax warpgroups take kSoftmaxRegs per thread and the third
+// warpgroup (producer, MMA issuer, two idle warps) kOtherRegs, with
+// 2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= 64512 (checked per config).
+constexpr int kLaunchRegs = 168;
 constexpr int kBM = 128;  // query rows per stage
 constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kDV = 128;
@@ -84,6 +91,12 @@ struct Cfg {
   static constexpr uint32_t kFmt = kF8 ? 0u : 1u;   // E4M3 / BF16
   static constexpr uint32_t kIdescQK = ptx::instr_desc(kFmt, kFmt, 0, kBM, kBN);
   static constexpr uint32_t kIdescPV = ptx::instr_desc(kFmt, kFmt, 1, kBM, kDV);
+  // Register split: the MMA issuer of the d_qk = 192 BF16 form unrolls 12
+  // K steps and needs more registers than the others.
+  static constexpr int kSoftmaxRegs = (!kF8 && DQK == 192) ? 192 : 200;
+  static constexpr int kOtherRegs = (!kF8 && DQK == 192) ? 120 : 104;
+  static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
+                "register split exceeds the launch allocation");
   static_assert(kNumSlots >= 2, "K/V ring needs at least two slots");
   static_assert(kSmemBytes <= kMaxDynSmem, "shared memory budget");
   static_assert(kSlotBytes % 1024 == 0 && kTileBytesQK % 1024 == 0, "1 KB alignment");
@@ -161,7 +174,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t b, uint32_t parity, volatile 
   ok = __shfl_sync(0xffffffffu, ok, 0);
   // Each lane observes the completed phase itself (an acquire of its own);
   // the phase cannot move on before this warp's next arrival.
-  if (ok) (void)ptx::mbar_try_wait(b, parity);
+  if (ok) (void)ptx::mbar_test(b, parity);
   return ok != 0;
 }
 
@@ -190,7 +203,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  auto bar = [&](int i) { return ptx::smem_u32(sm.bars + i); };
+  const uint32_t bars_smem = ptx::smem_u32(sm.bars);
+  const uint32_t q_smem = ptx::smem_u32(sm.q[0]);
+  const uint32_t slots_smem = ptx::smem_u32(sm.slots);
+  auto bar = [&](int i) { return bars_smem + 8u * static_cast<uint32_t>(i); };
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(B::kQFull + 0), 1);
@@ -233,30 +249,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int grid = gridDim.x;
   const int cta = blockIdx.x;
 
+  // Each setmaxnreg sits inside its role's branch so that the register
+  // allocator sees the softmax code only on the 224-register path.
+  if (warp >= 8) {
+    ptx::setmaxnreg_dec<C::kOtherRegs>();
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_q = ptx::policy_evict_first();
       const uint64_t pol_kv = ptx::policy_evict_last();
-      uint32_t q_uses[2] = {0, 0};
-      uint32_t t = 0;  // K/V tiles issued so far (ring position)
+      uint32_t q_par = 0;   // bit s: parity of the uses of Q buffer s so far
+      uint32_t q_used = 0;  // bit s: Q buffer s was loaded at least once
+      uint32_t t = 0;       // K/V tiles issued so far (ring position)
       const int group = p.H / p.Hkv;
       bool ok = true;
       for (int r = 0; ok; ++r) {
         const int w = item_index(r, cta, grid);
         if (w >= p.total_items) break;
         const Item it = decode_item(w, p);
-        for (int s = 0; s < 2 && ok; ++s) {
-          if (s == 1 && it.n1 == 0) break;
-          ok = ptx::mbar_wait(bar(B::kQEmpty + s), (q_uses[s] & 1u) ^ 1u, abort, status, 1);
+        const int nst = it.n1 > 0 ? 2 : 1;
+        for (int s = 0; s < nst && ok; ++s) {
+          ok = ptx::mbar_wait(bar(B::kQEmpty + s), ((q_par >> s) & 1u) ^ 1u, abort, status, 1);
           if (!ok) break;
           const uint32_t qb = bar(B::kQFull + s);
           ptx::mbar_arrive_expect_tx(qb, C::kTileBytesQK);
           const int row0 = (2 * it.u + s) * kBM;
+          const uint32_t qdst = q_smem + s * C::kTileBytesQK;
+#pragma unroll
           for (int c = 0; c < C::kChunksQK; ++c)
-            tma_tile(&tm_q, ptx::smem_u32(sm.q[s] + c * C::kChunkBytesQK), qb, p.layout,
-                     c * C::kChunkElemsQK, it.h, row0, it.b, pol_q);
-          ++q_uses[s];
+            tma_tile(&tm_q, qdst + c * C::kChunkBytesQK, qb, p.layout, c * C::kChunkElemsQK,
+                     it.h, row0, it.b, pol_q);
+          q_par ^= 1u << s;
+          q_used |= 1u << s;
         }
         const int hk = it.h / group;
         for (int j = 0; j < it.nload && ok; ++j) {
@@ -266,14 +290,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 1);
             if (!ok) break;
             const uint32_t fb = bar(B::kSlotFull + slot);
-            const uint32_t dst = ptx::smem_u32(sm.slots + slot * C::kSlotBytes);
+            const uint32_t dst = slots_smem + slot * C::kSlotBytes;
             if (kv == 0) {
               ptx::mbar_arrive_expect_tx(fb, C::kTileBytesQK);
+#pragma unroll
               for (int c = 0; c < C::kChunksQK; ++c)
                 tma_tile(&tm_k, dst + c * C::kChunkBytesQK, fb, p.layout,
                          c * C::kChunkElemsQK, hk, j * kBN, it.b, pol_kv);
             } else {
               ptx::mbar_arrive_expect_tx(fb, C::kTileBytesV);
+#pragma unroll
               for (int c = 0; c < C::kChunksV; ++c)
                 tma_tile(&tm_v, dst + c * C::kChunkBytesV, fb, p.layout, c * C::kChunkElemsV,
                          hk, j * kBN, it.b, pol_kv);
@@ -290,47 +316,46 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_drain(bar(B::kSlotFull + last % NS), (last / NS) & 1u);
         }
         for (int s = 0; s < 2; ++s)
-          if (q_uses[s]) ptx::mbar_drain(bar(B::kQFull + s), (q_uses[s] - 1) & 1u);
+          if ((q_used >> s) & 1u) ptx::mbar_drain(bar(B::kQFull + s), ((q_par >> s) & 1u) ^ 1u);
       }
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t q_uses[2] = {0, 0};
-      uint32_t p_uses[2] = {0, 0};
-      uint32_t pv_uses[2] = {0, 0};
+      uint32_t q_par = 0, p_par = 0, pv_par = 0;  // bit s: phase parity per stage
       uint32_t t = 0;
       bool ok = true;
-      const uint32_t tm_s[2] = {tmem + 0, tmem + 128};
-      const uint32_t tm_o[2] = {tmem + 256, tmem + 384};
-      const uint32_t q_addr[2] = {ptx::smem_u32(sm.q[0]), ptx::smem_u32(sm.q[1])};
-      const uint32_t slots_addr = ptx::smem_u32(sm.slots);
+      // Base descriptors; an MMA adds its byte offset >> 4 to the start
+      // address field (addresses stay below 256 KB, so no carry leaves it).
+      const uint64_t dq0 = ptx::smem_desc(q_smem, 16, 8 * C::kSwzQK, C::kSwzModeQK);
+      const uint64_t dk0 = ptx::smem_desc(slots_smem, 16, 8 * C::kSwzQK, C::kSwzModeQK);
+      const uint64_t dv0 = ptx::smem_desc(slots_smem, C::kChunkBytesV, 1024, 2u);
 
+      // S_s = Q_s K^T from K/V slot `slot`.
       auto issue_s = [&](int s, uint32_t slot) {
-        const uint32_t kaddr = slots_addr + slot * C::kSlotBytes;
+        const uint64_t dq = dq0 + ((s * C::kTileBytesQK) >> 4);
+        const uint64_t dk = dk0 + ((slot * C::kSlotBytes) >> 4);
+        const uint32_t d_tmem = tmem + s * 128;
 #pragma unroll
         for (int c = 0; c < C::kChunksQK; ++c) {
 #pragma unroll
           for (int kk = 0; kk < C::kSwzQK / 32; ++kk) {
-            const uint32_t off = c * C::kChunkBytesQK + kk * 32;
-            const uint64_t da = ptx::smem_desc(q_addr[s] + off, 16, 8 * C::kSwzQK, C::kSwzModeQK);
-            const uint64_t db = ptx::smem_desc(kaddr + off, 16, 8 * C::kSwzQK, C::kSwzModeQK);
-            ptx::mma_ss<C::kF8>(tm_s[s], da, db, C::kIdescQK, (c | kk) != 0);
+            const uint32_t off = (c * C::kChunkBytesQK + kk * 32) >> 4;
+            ptx::mma_ss<C::kF8>(d_tmem, dq + off, dk + off, C::kIdescQK, (c | kk) != 0);
           }
         }
       };
-      // O_s (+)= P V_j, with P read from tensor memory at column offset
-      // p_col of S_s (FP8 keeps a second, residual P term at offset 32).
+      // O_s (+)= P V with V in slot `slot` and P read from tensor memory at
+      // column offset p_col of S_s (FP8 keeps a residual P term at 32).
       auto issue_pv = [&](int s, uint32_t slot, bool acc_first, uint32_t p_col) {
-        const uint32_t vaddr = slots_addr + slot * C::kSlotBytes;
+        const uint64_t dv = dv0 + ((slot * C::kSlotBytes) >> 4);
+        const uint32_t a_tmem = tmem + s * 128 + p_col;
+        const uint32_t d_tmem = tmem + 256 + s * 128;
 #pragma unroll
-        for (int ks = 0; ks < kBN / C::kUmmaK; ++ks) {
-          const uint64_t db =
-              ptx::smem_desc(vaddr + ks * C::kUmmaK * 128, C::kChunkBytesV, 1024, 2u);
-          ptx::mma_ts<C::kF8>(tm_o[s], tm_s[s] + p_col + ks * 8, db, C::kIdescPV,
-                              (acc_first || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < kBN / C::kUmmaK; ++ks)
+          ptx::mma_ts<C::kF8>(d_tmem, a_tmem + ks * 8, dv + ((ks * C::kUmmaK * 128) >> 4),
+                              C::kIdescPV, (acc_first || ks > 0) ? 1u : 0u);
       };
 
       for (int r = 0; ok; ++r) {
@@ -339,8 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = decode_item(w, p);
         const int nst = it.n1 > 0 ? 2 : 1;
         for (int s = 0; s < nst && ok; ++s) {
-          ok = ptx::mbar_wait(bar(B::kQFull + s), q_uses[s] & 1u, abort, status, 1);
-          ++q_uses[s];
+          ok = ptx::mbar_wait(bar(B::kQFull + s), (q_par >> s) & 1u, abort, status, 1);
+          q_par ^= 1u << s;
         }
         if (!ok) break;
         // Prologue: S of K/V tile 0 for both stages.
@@ -374,9 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < 2; ++s) {
             const int ns = s == 0 ? it.n0 : it.n1;
             if (j >= ns) continue;
-            ok = ptx::mbar_wait(bar(B::kPFull + s), p_uses[s] & 1u, abort, status, 1);
+            ok = ptx::mbar_wait(bar(B::kPFull + s), (p_par >> s) & 1u, abort, status, 1);
             if (!ok) break;
-            ++p_uses[s];
+            p_par ^= 1u << s;
             ptx::tc_fence_after();
             issue_pv(s, slot_v, j > 0, 0);
             if (C::kF8 && j + 1 == ns) issue_pv(s, slot_v, true, 32);  // lo term of P
@@ -384,8 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               // Verification mode: P (aliasing S) is fully consumed before the
               // next S MMA of this stage overwrites it.
               ptx::mma_commit(bar(B::kPvDone + s));
-              ok = ptx::mbar_wait(bar(B::kPvDone + s), pv_uses[s] & 1u, abort, status, 1);
-              ++pv_uses[s];
+              ok = ptx::mbar_wait(bar(B::kPvDone + s), (pv_par >> s) & 1u, abort, status, 1);
+              pv_par ^= 1u << s;
               if (!ok) break;
             }
             if (j + 1 < ns) {
@@ -413,7 +438,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_drain(bar(B::kDrain), 0);
     }
     __syncwarp();
+  }
   } else {
+    ptx::setmaxnreg_inc<C::kSoftmaxRegs>();
     // ------------------------------------------------------------- softmax
     const int s = warp >> 2;            // stage
     const int wq = warp & 3;            // lane quarter of TMEM this warp may access
@@ -454,9 +481,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c > row_in_tile) f[c] = -INFINITY;
         }
-        float mx = f[0];
+        // Row maximum of the tile: eight independent chains of three-input
+        // max, so the reduction is not one 128-long dependency chain.
+        float m8[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, f[c]);
+        for (int a = 0; a < 8; ++a) {
+          float acc = ptx::max3(f[16 * a], f[16 * a + 1], f[16 * a + 2]);
+#pragma unroll
+          for (int k = 3; k < 15; k += 2) acc = ptx::max3(acc, f[16 * a + k], f[16 * a + k + 1]);
+          m8[a] = fmaxf(acc, f[16 * a + 15]);
+        }
+        float mx = ptx::max3(ptx::max3(m8[0], m8[1], m8[2]), ptx::max3(m8[3], m8[4], m8[5]),
+                             fmaxf(m8[6], m8[7]));
         mx *= c_log2;
         if (j == 0) {
           m_ref = mx;
@@ -481,69 +517,85 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tmem_wait_st();
           }
         }
+        // p = 2^(s*c - m_ref) (times 2^8 for FP8): paired multiply-adds and
+        // one exp2 each, processed in chunks of 32 columns that are packed
+        // and stored to tensor memory at once, so few values stay live.
         const float neg_m = C::kPLog2Scale - m_ref;
-        float rs = 0.f;
+        const float2 c2 = make_float2(c_log2, c_log2);
+        const float2 nm2 = make_float2(neg_m, neg_m);
+        // Whether one probability of this tile can carry 1/8 of the row's
+        // mass (p_max * 8 > l_old + p_max bounds p_max * 8 > l_new from
+        // above): only then can its rounding show in the normalised output,
+        // so only then is the denominator summed over the rounded values
+        // exactly; otherwise the tile's rounding errors average out and
+        // the unrounded tile sum stands in for the rounded one.
+        const bool heavy = __any_sync(0xffffffffu, ptx::ex2(mx + neg_m) * 7.0f > l);
+        const bool two_term = C::kF8 && j == tile;
+        float2 s4[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float e = ptx::ex2(fmaf(f[c], c_log2, neg_m));
-          rs += e;
-          f[c] = e;
-        }
-        l += rs;
-        if constexpr (C::kF8) {
-          uint32_t pk[32];
-          if (j != tile) {
-            uint32_t acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // FP16x2 partial sums of rounded P
+        for (int ch = 0; ch < 4; ++ch) {
+          float e[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              pk[i] = ptx::pack_e4m3x4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
-              ptx::add_e4m3x4_f16x2(pk[i], acc[2 * (i & 3)], acc[2 * (i & 3) + 1]);
+          for (int i = 0; i < 16; ++i) {
+            const float2 x = __ffma2_rn(make_float2(f[32 * ch + 2 * i], f[32 * ch + 2 * i + 1]),
+                                        c2, nm2);
+            e[2 * i] = ptx::ex2(x.x);
+            e[2 * i + 1] = ptx::ex2(x.y);
+            s4[i & 1] = __fadd2_rn(s4[i & 1], make_float2(e[2 * i], e[2 * i + 1]));
+          }
+          if constexpr (C::kF8) {
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              pk[i] = ptx::pack_e4m3x4(e[4 * i], e[4 * i + 1], e[4 * i + 2], e[4 * i + 3]);
+            ptx::tmem_st8(t_s + ch * 8, pk);
+            if (!two_term) {
+              uint32_t acc[2] = {0u, 0u};
+#pragma unroll
+              for (int i = 0; i < 8; ++i) ptx::add_e4m3x4_f16x2(pk[i], acc[0], acc[1]);
+              r4[ch] = ptx::f16x2_sum_f32(acc[0]) + ptx::f16x2_sum_f32(acc[1]);
+            } else {
+              // Diagonal tile: its rows see few keys (row i of the first
+              // tile sees i + 1), so one e4m3 rounding of a probability shows
+              // in the output.  P is stored as two e4m3 terms, hi + lo, lo
+              // being the rounding residual of hi; the MMA issuer adds a
+              // second P V product for lo (P then has about 8 significant
+              // bits on this tile).
+              uint32_t lo[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                float d[4], q[4];
+                ptx::unpack_e4m3x4(pk[i], d);
+                lo[i] = ptx::pack_e4m3x4(e[4 * i] - d[0], e[4 * i + 1] - d[1],
+                                         e[4 * i + 2] - d[2], e[4 * i + 3] - d[3]);
+                ptx::unpack_e4m3x4(lo[i], q);
+                r4[ch] += ((d[0] + q[0]) + (d[1] + q[1])) + ((d[2] + q[2]) + (d[3] + q[3]));
+              }
+              ptx::tmem_st8(t_s + 32 + ch * 8, lo);
             }
-            ptx::tmem_st32(t_s, pk);
-            float rr = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) rr += ptx::f16x2_sum_f32(acc[i]);
-            lr += rr;
           } else {
-            // Diagonal tile: its rows see few keys (row i of the first tile
-            // sees i + 1), so one e4m3 rounding of a probability shows in
-            // the output.  P is stored as two e4m3 terms, hi + lo, where lo
-            // is the rounding residual of hi; the MMA issuer adds a second
-            // P V product for lo, giving P about 8 significant bits here.
-            uint32_t lo[32];
-            float rr = 0.f;
+            uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              pk[i] = ptx::pack_e4m3x4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
-              float d[4];
-              ptx::unpack_e4m3x4(pk[i], d);
-              lo[i] = ptx::pack_e4m3x4(f[4 * i] - d[0], f[4 * i + 1] - d[1],
-                                       f[4 * i + 2] - d[2], f[4 * i + 3] - d[3]);
-              float e[4];
-              ptx::unpack_e4m3x4(lo[i], e);
-              rr += (d[0] + e[0]) + (d[1] + e[1]) + (d[2] + e[2]) + (d[3] + e[3]);
+            for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(e[2 * i], e[2 * i + 1]);
+            ptx::tmem_st16(t_s + ch * 16, pk);
+            if (heavy) {
+              // Denominator over the same rounded probabilities that multiply
+              // V, so the output weights sum to one (ZYFA README, "Accuracy").
+              float r2[2] = {0.f, 0.f};
+#pragma unroll
+              for (int i = 0; i < 16; ++i) r2[i & 1] = ptx::add_bf16x2_f32(r2[i & 1], pk[i]);
+              r4[ch] = r2[0] + r2[1];
             }
-            ptx::tmem_st32(t_s, pk);
-            ptx::tmem_st32(t_s + 32, lo);
-            lr += rr;
           }
-        } else {
-          // BF16: the denominator of O is the sum of the same rounded
-          // probabilities that multiply V, so the output weights sum to one
-          // (ZYFA README, "Accuracy"); a BF16 pair unpacks exactly by shifts.
-          float rr = 0.f;
-#pragma unroll
-          for (int h2 = 0; h2 < 2; ++h2) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              pk[i] = ptx::pack_bf16x2(f[64 * h2 + 2 * i], f[64 * h2 + 2 * i + 1]);
-              rr += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
-            }
-            ptx::tmem_st32(t_s + h2 * 32, pk);
-          }
-          lr += rr;
         }
+        const float2 s2 = __fadd2_rn(s4[0], s4[1]);
+        const float rs = s2.x + s2.y;
+        l += rs;
+        if (C::kF8 || heavy)
+          lr += (r4[0] + r4[1]) + (r4[2] + r4[3]);
+        else
+          lr += rs;
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
