@@ -138,6 +138,7 @@ struct Smem {
   uint64_t* bars;
   uint32_t* tmem_base;
   int* abort;
+  volatile uint32_t* pflag;   // [stage]: index of the last tile with a two-term FP8 P
 };
 
 // Barrier indices inside the barrier array.
@@ -199,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.bars = reinterpret_cast<uint64_t*>(sm.slots + NS * C::kSlotBytes);
   sm.tmem_base = reinterpret_cast<uint32_t*>(sm.bars + B::kCount);
   sm.abort = reinterpret_cast<int*>(sm.tmem_base + 1);
+  sm.pflag = reinterpret_cast<volatile uint32_t*>(sm.abort + 1);
   volatile int* abort = sm.abort;
 
   const int warp = threadIdx.x >> 5;
@@ -227,6 +229,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(B::kSlotEmpty + i), 1);
     }
     *sm.abort = 0;
+    sm.pflag[0] = 0;
+    sm.pflag[1] = 0;
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
   }
@@ -324,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t q_par = 0, p_par = 0, pv_par = 0;  // bit s: phase parity per stage
+      uint32_t p_count[2] = {0u, 0u};             // P tiles received per stage
       uint32_t t = 0;
       bool ok = true;
       // Base descriptors; an MMA adds its byte offset >> 4 to the start
@@ -402,9 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = ptx::mbar_wait(bar(B::kPFull + s), (p_par >> s) & 1u, abort, status, 1);
             if (!ok) break;
             p_par ^= 1u << s;
+            ++p_count[s];
             ptx::tc_fence_after();
             issue_pv(s, slot_v, j > 0, 0);
-            if (C::kF8 && j + 1 == ns) issue_pv(s, slot_v, true, 32);  // lo term of P
+            if (C::kF8 && sm.pflag[s] == p_count[s]) issue_pv(s, slot_v, true, 32);  // lo term
             if (p.serialize_pv && j + 1 < ns) {
               // Verification mode: P (aliasing S) is fully consumed before the
               // next S MMA of this stage overwrites it.
@@ -529,8 +535,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         // so only then is the denominator summed over the rounded values
         // exactly; otherwise the tile's rounding errors average out and
         // the unrounded tile sum stands in for the rounded one.
-        const bool heavy = __any_sync(0xffffffffu, ptx::ex2(mx + neg_m) * 7.0f > l);
-        const bool two_term = C::kF8 && j == tile;
+        const float p_max = ptx::ex2(mx + neg_m);
+        const bool heavy = __any_sync(0xffffffffu, p_max * 7.0f > l);
+        // FP8: a probability that can carry 1/32 of the row's mass (or any
+        // on the diagonal tile, whose rows see few keys) would show its e4m3
+        // rounding (up to 2^-4 relative) in the output, so such tiles keep P
+        // as two e4m3 terms, hi + lo (lo = rounding residual of hi, about 8
+        // significant bits together).  The MMA issuer adds a second P V
+        // product for lo when any warp of the stage flags the tile; the
+        // other warps store zeros as their lo term.
+        const bool two_term =
+            C::kF8 && (j == tile || __any_sync(0xffffffffu, p_max * 31.0f > l));
+        if (C::kF8) {
+          if (two_term) {
+            if (lane == 0) sm.pflag[s] = s_uses;
+          } else {
+            const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int c = 0; c < 4; ++c) ptx::tmem_st8(t_s + 32 + c * 8, z);
+          }
+        }
         float2 s4[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -556,12 +580,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int i = 0; i < 8; ++i) ptx::add_e4m3x4_f16x2(pk[i], acc[0], acc[1]);
               r4[ch] = ptx::f16x2_sum_f32(acc[0]) + ptx::f16x2_sum_f32(acc[1]);
             } else {
-              // Diagonal tile: its rows see few keys (row i of the first
-              // tile sees i + 1), so one e4m3 rounding of a probability shows
-              // in the output.  P is stored as two e4m3 terms, hi + lo, lo
-              // being the rounding residual of hi; the MMA issuer adds a
-              // second P V product for lo (P then has about 8 significant
-              // bits on this tile).
               uint32_t lo[8];
 #pragma unroll
               for (int i = 0; i < 8; ++i) {

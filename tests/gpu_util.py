@@ -36,13 +36,29 @@ def device_inputs(t: dict, w: workloads.Workload):
     return q, k, v, ds
 
 
-def run_gpu(t: dict, w: workloads.Workload, scale=None):
-    """O (caller's layout) and LSE (B,H,S) from the CUDA path, as float64."""
+def run_gpu(t: dict, w: workloads.Workload, scale=None, rows=None, heads=None):
+    """O and LSE from the CUDA path, as float64.
+
+    Without ``rows``/``heads``: O in the caller's layout and LSE (B,H,S).
+    With them: only those query rows and heads, O as (B,H',R,dv) and LSE as
+    (B,H',R), selected on the device before the copy to the host.
+    """
     q, k, v, ds = device_inputs(t, w)
     out, lse = zf.attention(q, k, v, q_descale=ds[0], k_descale=ds[1], v_descale=ds[2],
                             softmax_scale=scale, layout=w.layout, return_lse=True)
     torch.cuda.synchronize()
-    return out.float().cpu().double().numpy(), lse.cpu().double().numpy()
+    if rows is None and heads is None:
+        return out.float().cpu().double().numpy(), lse.cpu().double().numpy()
+    r = torch.as_tensor(np.asarray(rows), device=out.device)
+    h = torch.as_tensor(np.asarray(heads), device=out.device)
+    if w.layout == "bshd":
+        o = out.index_select(1, r).index_select(2, h).transpose(1, 2)
+    else:
+        o = out.index_select(1, h).index_select(2, r)
+    lsel = lse.index_select(1, h).index_select(2, r)
+    res = o.float().cpu().double().numpy(), lsel.cpu().double().numpy()
+    del q, k, v, out, lse
+    return res
 
 
 def run_oracle(t: dict, w: workloads.Workload, rows=None, scale=None, heads=None):

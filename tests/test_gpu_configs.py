@@ -1,0 +1,62 @@
+"""Parity at the full sizes of the named workloads, in the launch
+configuration bench.py times.
+
+The oracle computes only sampled query rows (rows 0..255, every 128-row
+tile boundary +-1, the last 256 rows and 512 seeded random rows) of sampled
+(batch, head) pairs, from the same definition restricted to those rows; the
+GPU computes the whole problem.  The sample and the tolerances are stated in
+gpu_util (specification bounds, with the BF16-output faithful-rounding
+reading for |O| >= 4).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from gpu_util import assert_parity, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+W = workloads.WORKLOADS
+
+FULL = [
+    "bf16_mha_b1_h2_s256_d128",
+    "bf16_gqa_b1_h32kv8_s8192_d128",
+    "fp8_gqa_b1_h32kv8_s16384_d128",
+    "bf16_gqa_b1_h32kv8_s16384_d128",
+    "bf16_mla_b1_h16_s16384_d192",
+    "fp8_mla_b1_h16_s16384_d192",
+] + [f"{dt}_mha_b2_h32_s{S}_d128" for dt in ("bf16", "fp8")
+     for S in (2048, 4096, 16384, 30000, 32768)]
+
+
+def _heads(w):
+    """(batch, head) pairs to check: first, last, and one from the middle of
+    a KV group, in every batch."""
+    hs = sorted({0, w.H - 1, min(w.H - 1, w.H // 2 + 1)})
+    return hs
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows(name):
+    w = W[name]
+    t = workloads.make_inputs(w)
+    rows = workloads.sample_rows(w.S, seed=w.seed)
+    heads = _heads(w)
+    Og, Lg = run_gpu(t, w, rows=rows, heads=heads)
+    torch.cuda.empty_cache()
+    Oref, Lref = run_oracle(t, w, rows=rows, heads=heads)
+    assert_parity(Og, Lg, Oref, Lref, w.dtype,
+                  f"{name} rows={len(rows)} heads={heads} batches={w.B}")
+
+
+@pytest.mark.parametrize("name", ["bf16_gqa_b1_h32kv8_s16384_d128",
+                                  "fp8_gqa_b1_h32kv8_s16384_d128"])
+def test_full_size_deterministic(name):
+    w = W[name]
+    t = workloads.make_inputs(w)
+    O1, L1 = run_gpu(t, w)
+    for _ in range(2):
+        O2, L2 = run_gpu(t, w)
+        assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
