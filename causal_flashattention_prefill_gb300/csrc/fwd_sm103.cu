@@ -81,13 +81,15 @@ struct Cfg {
   static constexpr int kSlotsFit = (kMaxDynSmem - kReserve - 2 * kTileBytesQK) / kSlotBytes;
   static constexpr int kNumSlots = kSlotsFit > 8 ? 8 : kSlotsFit;
   static constexpr int kSmemBytes = kReserve + 2 * kTileBytesQK + kNumSlots * kSlotBytes;
-  // Lazy-rescale threshold in base-2 units of the score (ZYFA README,
-  // "Kernel design": 0.125 for FP8; BF16 keeps an FP32 accumulator with
-  // headroom, so it uses 8 as the CDNA4 post does).
-  static constexpr float kTau = kF8 ? 0.125f : 8.0f;
-  // FP8 P is stored as e4m3 of p * 2^8 (p <= 2^tau keeps it below 448); the
-  // factor enters as +8 in the exponent.
-  static constexpr float kPLog2Scale = kF8 ? 8.0f : 0.0f;
+  // Lazy-rescale threshold in base-2 units of the score (the ZYFA README's
+  // "Kernel design" uses 0.125-8).  Large thresholds keep the reference
+  // from moving after the first tiles, so exp2 can run against it before
+  // the tile maximum is known: BF16 8 (p <= 256), FP8 4 (p * 2^4 <= 256,
+  // inside e4m3's 448).
+  static constexpr float kTau = kF8 ? 4.0f : 8.0f;
+  // FP8 P is stored as e4m3 of p * 2^4 (p <= 2^tau keeps it below 448); the
+  // factor enters as +4 in the exponent.
+  static constexpr float kPLog2Scale = kF8 ? 4.0f : 0.0f;
   static constexpr uint32_t kFmt = kF8 ? 0u : 1u;   // E4M3 / BF16
   static constexpr uint32_t kIdescQK = ptx::instr_desc(kFmt, kFmt, 0, kBM, kBN);
   static constexpr uint32_t kIdescPV = ptx::instr_desc(kFmt, kFmt, 1, kBM, kDV);
@@ -177,6 +179,136 @@ __device__ __forceinline__ bool warp_wait(uint32_t b, uint32_t parity, volatile 
   // the phase cannot move on before this warp's next arrival.
   if (ok) (void)ptx::mbar_test(b, parity);
   return ok != 0;
+}
+
+// Maximum of 64 / 128 scores: independent chains of three-input max.
+__device__ __forceinline__ float row_max64(const float* f) {
+  float m4[4];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    float acc = ptx::max3(f[16 * a], f[16 * a + 1], f[16 * a + 2]);
+#pragma unroll
+    for (int k = 3; k < 15; k += 2) acc = ptx::max3(acc, f[16 * a + k], f[16 * a + k + 1]);
+    m4[a] = fmaxf(acc, f[16 * a + 15]);
+  }
+  return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+
+__device__ __forceinline__ float row_max128(const float* f) {
+  return fmaxf(row_max64(f), row_max64(f + 64));
+}
+
+// P for 64 scores (half h of the row): p = 2^(s*c + neg_m) by paired FMAs
+// and exp2, packed to BF16 (or e4m3; with two_term also the e4m3 rounding
+// residual at column offset 32), stored to tensor memory over S.  `sacc`
+// accumulates the unrounded sum; with kExact (BF16) `rr` accumulates the sum
+// of the rounded values that multiply V.
+template <class C, bool kExact>
+__device__ __forceinline__ void produce_half(const float* f, float c_log2, float neg_m,
+                                             uint32_t t_s, int h, bool two_term,
+                                             float2 (&sacc)[2], float& rr) {
+  const float2 c2 = make_float2(c_log2, c_log2);
+  const float2 nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+  for (int cc = 0; cc < 2; ++cc) {
+    const int ch = 2 * h + cc;  // 32-column chunk of the row
+    float e[32];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 x = __ffma2_rn(make_float2(f[32 * ch + 2 * i], f[32 * ch + 2 * i + 1]), c2, nm2);
+      e[2 * i] = ptx::ex2(x.x);
+      e[2 * i + 1] = ptx::ex2(x.y);
+      sacc[i & 1] = __fadd2_rn(sacc[i & 1], make_float2(e[2 * i], e[2 * i + 1]));
+    }
+    if constexpr (C::kF8) {
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        pk[i] = ptx::pack_e4m3x4(e[4 * i], e[4 * i + 1], e[4 * i + 2], e[4 * i + 3]);
+      ptx::tmem_st8(t_s + ch * 8, pk);
+      if (two_term) {
+        uint32_t lo[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          float d[4];
+          ptx::unpack_e4m3x4(pk[i], d);
+          lo[i] = ptx::pack_e4m3x4(e[4 * i] - d[0], e[4 * i + 1] - d[1], e[4 * i + 2] - d[2],
+                                   e[4 * i + 3] - d[3]);
+        }
+        ptx::tmem_st8(t_s + 32 + ch * 8, lo);
+      }
+    } else {
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(e[2 * i], e[2 * i + 1]);
+      ptx::tmem_st16(t_s + ch * 16, pk);
+      if constexpr (kExact) {
+        float a2[2] = {0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a2[i & 1] = ptx::add_bf16x2_f32(a2[i & 1], pk[i]);
+        rr += a2[0] + a2[1];
+      }
+    }
+  }
+}
+
+// FP8: the e4m3 rounding residual of P (lo term) for the 128 scores of the
+// row, recomputed from the scores exactly as the hi term was, stored at
+// column offset 32 of S.
+template <class C>
+__device__ __forceinline__ void store_lo_fp8(const float* f, float c_log2, float neg_m,
+                                             uint32_t t_s) {
+  const float2 c2 = make_float2(c_log2, c_log2);
+  const float2 nm2 = make_float2(neg_m, neg_m);
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 xa = __ffma2_rn(make_float2(f[32 * ch + 4 * i], f[32 * ch + 4 * i + 1]), c2, nm2);
+      const float2 xb =
+          __ffma2_rn(make_float2(f[32 * ch + 4 * i + 2], f[32 * ch + 4 * i + 3]), c2, nm2);
+      const float e0 = ptx::ex2(xa.x), e1 = ptx::ex2(xa.y), e2 = ptx::ex2(xb.x),
+                  e3 = ptx::ex2(xb.y);
+      float d[4];
+      ptx::unpack_e4m3x4(ptx::pack_e4m3x4(e0, e1, e2, e3), d);
+      lo[i] = ptx::pack_e4m3x4(e0 - d[0], e1 - d[1], e2 - d[2], e3 - d[3]);
+    }
+    ptx::tmem_st8(t_s + 32 + ch * 8, lo);
+  }
+}
+
+// BF16: the sum of the rounded P of the row (the values that multiply V),
+// recomputed from the scores exactly as P was.
+__device__ __forceinline__ float rounded_sum_bf16(const float* f, float c_log2, float neg_m) {
+  const float2 c2 = make_float2(c_log2, c_log2);
+  const float2 nm2 = make_float2(neg_m, neg_m);
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const float2 x = __ffma2_rn(make_float2(f[2 * i], f[2 * i + 1]), c2, nm2);
+    a[i & 3] = ptx::add_bf16x2_f32(a[i & 3], ptx::pack_bf16x2(ptx::ex2(x.x), ptx::ex2(x.y)));
+  }
+  return (a[0] + a[1]) + (a[2] + a[3]);
+}
+
+// P for the whole 128-score row against reference neg_m; rs = unrounded
+// sum, rr = sum of the rounded values (when `heavy`, BF16).
+template <class C>
+__device__ __forceinline__ void produce_tile(const float* f, float c_log2, float neg_m,
+                                             uint32_t t_s, bool heavy, bool two_term, float& rs,
+                                             float& rr) {
+  float2 sacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  rr = 0.f;
+  if (heavy) {
+    produce_half<C, true>(f, c_log2, neg_m, t_s, 0, two_term, sacc, rr);
+    produce_half<C, true>(f, c_log2, neg_m, t_s, 1, two_term, sacc, rr);
+  } else {
+    produce_half<C, false>(f, c_log2, neg_m, t_s, 0, two_term, sacc, rr);
+    produce_half<C, false>(f, c_log2, neg_m, t_s, 1, two_term, sacc, rr);
+  }
+  const float2 t2 = __fadd2_rn(sacc[0], sacc[1]);
+  rs = t2.x + t2.y;
 }
 
 }  // namespace
@@ -478,31 +610,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++s_uses;
         ptx::tc_fence_after();
+        // S row: columns 0..63 are loaded and waited for; 64..127 are
+        // requested at once and waited for after the first half's exp2.
         uint32_t v[128];
-        ptx::tmem_ld128_wait(t_s, v);
+        ptx::tmem_ld64_wait(t_s, *reinterpret_cast<uint32_t(*)[64]>(&v[0]));
+        ptx::tmem_ld64_nowait(t_s + 64, *reinterpret_cast<uint32_t(*)[64]>(&v[64]));
         float* f = reinterpret_cast<float*>(v);
-        if (j == tile) {
-          // Diagonal tile: key (row_in_tile + d) for d > 0 is in the future.
+        const bool diag = j == tile;
+        if (diag) {
+          // Diagonal tile: key column c is in the future of the row when
+          // c exceeds the row's index in the tile.
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
+          for (int c = 0; c < 64; ++c)
             if (c > row_in_tile) f[c] = -INFINITY;
         }
-        // Row maximum of the tile: eight independent chains of three-input
-        // max, so the reduction is not one 128-long dependency chain.
-        float m8[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-          float acc = ptx::max3(f[16 * a], f[16 * a + 1], f[16 * a + 2]);
-#pragma unroll
-          for (int k = 3; k < 15; k += 2) acc = ptx::max3(acc, f[16 * a + k], f[16 * a + k + 1]);
-          m8[a] = fmaxf(acc, f[16 * a + 15]);
-        }
-        float mx = ptx::max3(ptx::max3(m8[0], m8[1], m8[2]), ptx::max3(m8[3], m8[4], m8[5]),
-                             fmaxf(m8[6], m8[7]));
-        mx *= c_log2;
+        // Accuracy of the rounded P (decided per warp from the tile's actual
+        // maximum): a probability that carries at least 1/8 (BF16) or 1/32
+        // (FP8) of the row's mass so far would show its rounding in the
+        // normalised output.  BF16 then sums the denominator over the same
+        // rounded values that multiply V (ZYFA README, "Accuracy"); FP8
+        // keeps P as two e4m3 terms, hi + lo, lo being the rounding residual
+        // of hi (about 8 significant bits together; also on every diagonal
+        // tile, whose rows see few keys), and the MMA issuer adds a second
+        // P V product for lo when any warp of the stage flags the tile (the
+        // other warps store zeros as their lo term).  On other tiles the
+        // rounding errors average out and the unrounded sum stands in.
+        float rs = 0.f, rr = 0.f;
+        bool exact = false, two_term = false;
         if (j == 0) {
-          m_ref = mx;
+          // First tile of the row: the reference is this tile's maximum.
+          ptx::tmem_wait_ld_dep64(*reinterpret_cast<uint32_t(*)[64]>(&v[64]));
+          if (diag) {
+#pragma unroll
+            for (int c = 64; c < 128; ++c)
+              if (c > row_in_tile) f[c] = -INFINITY;
+          }
+          m_ref = row_max128(f) * c_log2;
+          exact = !C::kF8;
+          two_term = C::kF8;
+          produce_tile<C>(f, c_log2, C::kPLog2Scale - m_ref, t_s, exact, two_term, rs, rr);
         } else {
+          // Exp2 against the current reference while the tile maximum is
+          // formed; a tile whose maximum passes the reference by more than
+          // tau is recomputed after the rescale (rare: tau is large).
+          float neg_m = C::kPLog2Scale - m_ref;
+          float2 sacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+          const float m_lo = row_max64(f);
+          produce_half<C, false>(f, c_log2, neg_m, t_s, 0, false, sacc, rr);
+          ptx::tmem_wait_ld_dep64(*reinterpret_cast<uint32_t(*)[64]>(&v[64]));
+          if (diag) {
+#pragma unroll
+            for (int c = 64; c < 128; ++c)
+              if (c > row_in_tile) f[c] = -INFINITY;
+          }
+          const float m_hi = row_max64(f + 64);
+          produce_half<C, false>(f, c_log2, neg_m, t_s, 1, false, sacc, rr);
+          const float2 t2 = __fadd2_rn(sacc[0], sacc[1]);
+          rs = t2.x + t2.y;
+          const float mx = fmaxf(m_lo, m_hi) * c_log2;
           const bool need = mx > m_ref + C::kTau;
           if (__any_sync(0xffffffffu, need)) {
             const float alpha = need ? ptx::ex2(m_ref - mx) : 1.0f;
@@ -520,32 +685,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
               ptx::tmem_st32(t_o + c * 32, o);
             }
+            // P of this tile again, against the moved reference (exactly
+            // the values a non-speculative pass would have produced), after
+            // the speculative stores to the same columns have completed.
             ptx::tmem_wait_st();
+            neg_m = C::kPLog2Scale - m_ref;
+            produce_tile<C>(f, c_log2, neg_m, t_s, false, false, rs, rr);
+          }
+          const float p_max = ptx::ex2(mx + neg_m);   // largest p of the tile (x pre-scale)
+          if constexpr (C::kF8) {
+            two_term = diag || __any_sync(0xffffffffu, p_max * 32.0f > l + rs);
+            if (two_term) store_lo_fp8<C>(f, c_log2, neg_m, t_s);
+          } else {
+            exact = __any_sync(0xffffffffu, p_max * 8.0f > l + rs);
+            if (exact) rr = rounded_sum_bf16(f, c_log2, neg_m);
           }
         }
-        // p = 2^(s*c - m_ref) (times 2^8 for FP8): paired multiply-adds and
-        // one exp2 each, processed in chunks of 32 columns that are packed
-        // and stored to tensor memory at once, so few values stay live.
-        const float neg_m = C::kPLog2Scale - m_ref;
-        const float2 c2 = make_float2(c_log2, c_log2);
-        const float2 nm2 = make_float2(neg_m, neg_m);
-        // Whether one probability of this tile can carry 1/8 of the row's
-        // mass (p_max * 8 > l_old + p_max bounds p_max * 8 > l_new from
-        // above): only then can its rounding show in the normalised output,
-        // so only then is the denominator summed over the rounded values
-        // exactly; otherwise the tile's rounding errors average out and
-        // the unrounded tile sum stands in for the rounded one.
-        const float p_max = ptx::ex2(mx + neg_m);
-        const bool heavy = __any_sync(0xffffffffu, p_max * 7.0f > l);
-        // FP8: a probability that can carry 1/32 of the row's mass (or any
-        // on the diagonal tile, whose rows see few keys) would show its e4m3
-        // rounding (up to 2^-4 relative) in the output, so such tiles keep P
-        // as two e4m3 terms, hi + lo (lo = rounding residual of hi, about 8
-        // significant bits together).  The MMA issuer adds a second P V
-        // product for lo when any warp of the stage flags the tile; the
-        // other warps store zeros as their lo term.
-        const bool two_term =
-            C::kF8 && (j == tile || __any_sync(0xffffffffu, p_max * 31.0f > l));
         if (C::kF8) {
           if (two_term) {
             if (lane == 0) sm.pflag[s] = s_uses;
@@ -555,65 +710,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < 4; ++c) ptx::tmem_st8(t_s + 32 + c * 8, z);
           }
         }
-        float2 s4[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        float r4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float e[32];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 x = __ffma2_rn(make_float2(f[32 * ch + 2 * i], f[32 * ch + 2 * i + 1]),
-                                        c2, nm2);
-            e[2 * i] = ptx::ex2(x.x);
-            e[2 * i + 1] = ptx::ex2(x.y);
-            s4[i & 1] = __fadd2_rn(s4[i & 1], make_float2(e[2 * i], e[2 * i + 1]));
-          }
-          if constexpr (C::kF8) {
-            uint32_t pk[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              pk[i] = ptx::pack_e4m3x4(e[4 * i], e[4 * i + 1], e[4 * i + 2], e[4 * i + 3]);
-            ptx::tmem_st8(t_s + ch * 8, pk);
-            if (!two_term) {
-              uint32_t acc[2] = {0u, 0u};
-#pragma unroll
-              for (int i = 0; i < 8; ++i) ptx::add_e4m3x4_f16x2(pk[i], acc[0], acc[1]);
-              r4[ch] = ptx::f16x2_sum_f32(acc[0]) + ptx::f16x2_sum_f32(acc[1]);
-            } else {
-              uint32_t lo[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                float d[4], q[4];
-                ptx::unpack_e4m3x4(pk[i], d);
-                lo[i] = ptx::pack_e4m3x4(e[4 * i] - d[0], e[4 * i + 1] - d[1],
-                                         e[4 * i + 2] - d[2], e[4 * i + 3] - d[3]);
-                ptx::unpack_e4m3x4(lo[i], q);
-                r4[ch] += ((d[0] + q[0]) + (d[1] + q[1])) + ((d[2] + q[2]) + (d[3] + q[3]));
-              }
-              ptx::tmem_st8(t_s + 32 + ch * 8, lo);
-            }
-          } else {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(e[2 * i], e[2 * i + 1]);
-            ptx::tmem_st16(t_s + ch * 16, pk);
-            if (heavy) {
-              // Denominator over the same rounded probabilities that multiply
-              // V, so the output weights sum to one (ZYFA README, "Accuracy").
-              float r2[2] = {0.f, 0.f};
-#pragma unroll
-              for (int i = 0; i < 16; ++i) r2[i & 1] = ptx::add_bf16x2_f32(r2[i & 1], pk[i]);
-              r4[ch] = r2[0] + r2[1];
-            }
-          }
-        }
-        const float2 s2 = __fadd2_rn(s4[0], s4[1]);
-        const float rs = s2.x + s2.y;
         l += rs;
-        if (C::kF8 || heavy)
-          lr += (r4[0] + r4[1]) + (r4[2] + r4[3]);
-        else
-          lr += rs;
+        lr += exact ? rr : rs;
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
