@@ -17,11 +17,14 @@ from ._lib import (  # noqa: F401
     ZYFA_ERR_DEVICE_TIMEOUT,
     ZYFA_ERR_LAUNCH,
     ZYFA_ERR_UNSUPPORTED,
+    ZYFA_F32,
     ZYFA_FP8_E4M3,
     ZYFA_OK,
     ZYFA_OPT_SERIALIZE_PV,
     load,
     zyfa_device_status,
+    zyfa_fp8_quantize,
+    zyfa_fp8_quantize_workspace_bytes,
     zyfa_fwd,
     zyfa_fwd_scaled,
     zyfa_set_option,

@@ -23,6 +23,7 @@ ZYFA_ERR_DEVICE_TIMEOUT = -6
 
 ZYFA_BF16 = 0
 ZYFA_FP8_E4M3 = 1
+ZYFA_F32 = 2
 ZYFA_BSHD = 0
 ZYFA_BHSD = 1
 ZYFA_OPT_SERIALIZE_PV = 1
@@ -40,6 +41,8 @@ SIGNATURES = {
     "zyfa_device_status": (_I, [ctypes.POINTER(_I), _I]),
     "zyfa_set_option": (_I, [_I, _I]),
     "zyfa_version": (_I, []),
+    "zyfa_fp8_quantize": (_I, [_P, ctypes.c_longlong, _I, _P, _P, _P, _P]),
+    "zyfa_fp8_quantize_workspace_bytes": (ctypes.c_longlong, []),
 }
 
 _lib = None
@@ -99,3 +102,11 @@ def zyfa_set_option(option: int, value: int) -> int:
 
 def zyfa_version() -> int:
     return load().zyfa_version()
+
+
+def zyfa_fp8_quantize(x, n, x_dtype, x8, descale, workspace, stream) -> int:
+    return load().zyfa_fp8_quantize(x, n, x_dtype, x8, descale, workspace, stream)
+
+
+def zyfa_fp8_quantize_workspace_bytes() -> int:
+    return load().zyfa_fp8_quantize_workspace_bytes()

@@ -76,16 +76,32 @@ def attention(q, k, v, out=None, lse=None, q_descale=None, k_descale=None, v_des
     return (out, lse) if return_lse else out
 
 
-def fp8_quantize(x: torch.Tensor):
-    """Per-tensor e4m3 quantisation with a power-of-two descale.
+def fp8_quantize(x: torch.Tensor, workspace: torch.Tensor = None, stream=None):
+    """Per-tensor e4m3 quantisation with a power-of-two descale, on the GPU.
 
-    Returns ``(x8, descale)`` with ``descale`` a 1-element float32 tensor on
-    ``x``'s device, ``2**ceil(log2(max|x| / 448))``, so the call never waits
-    for the host (ZYFA README, "Usage").
+    Returns ``(x8, descale)``: ``x8`` a ``float8_e4m3fn`` tensor shaped like
+    ``x`` and ``descale`` a 1-element float32 tensor on ``x``'s device,
+    ``2**ceil(log2(max|x| / 448))``; the call never waits for the host
+    (ZYFA README, "Usage").  ``x`` is BF16 or float32, contiguous.
     """
-    amax = x.detach().abs().amax().float().clamp_min(torch.finfo(torch.float32).tiny)
-    descale = torch.exp2(torch.ceil(torch.log2(amax / 448.0))).reshape(1)
-    x8 = (x.detach().float() / descale).to(torch.float8_e4m3fn)
+    if x.dtype == torch.bfloat16:
+        xt = _lib.ZYFA_BF16
+    elif x.dtype == torch.float32:
+        xt = _lib.ZYFA_F32
+    else:
+        raise TypeError(f"fp8_quantize takes BF16 or float32, not {x.dtype}")
+    x = x.detach().contiguous()
+    x8 = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=x.device)
+    descale = torch.empty(1, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(_lib.zyfa_fp8_quantize_workspace_bytes(), dtype=torch.uint8,
+                                device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    st = _lib.zyfa_fp8_quantize(x.data_ptr(), x.numel(), xt, x8.data_ptr(), descale.data_ptr(),
+                                workspace.data_ptr(), stream)
+    if st != _lib.ZYFA_OK:
+        raise ZyfaError(st)
     return x8, descale
 
 

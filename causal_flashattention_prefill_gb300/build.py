@@ -27,8 +27,8 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                      "-Xcompiler", "-fvisibility=hidden", "-diag-suppress", "177"]
 
-SOURCES = ["api.cpp", "fwd_sm103.cu"]
-HEADERS = ["fwd.h", "zyfa_ptx.cuh"]
+SOURCES = ["api.cpp", "fwd_sm103.cu", "quant.cu"]
+HEADERS = ["fwd.h", "quant.h", "zyfa_ptx.cuh"]
 
 
 def nvcc() -> str:

@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include "fwd.h"
+#include "quant.h"
 #include "zyfa.h"
 
 namespace {
@@ -223,6 +224,25 @@ int zyfa_set_option(int option, int value) {
   return ZYFA_ERR_ARG;
 }
 
-int zyfa_version(void) { return (1 << 16) | 0; }
+long long zyfa_fp8_quantize_workspace_bytes(void) {
+  return static_cast<long long>(zyfa::kQuantMaxPartials) * sizeof(float);
+}
+
+int zyfa_fp8_quantize(const void* x, long long n, int x_dtype, void* x8, float* descale,
+                      void* workspace, struct CUstream_st* stream) {
+  if (!x || !x8 || !descale || !workspace || n < 0) return ZYFA_ERR_ARG;
+  if (x_dtype != ZYFA_BF16 && x_dtype != ZYFA_F32) return ZYFA_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(x8, 8) || !aligned(descale, 4) || !aligned(workspace, 4))
+    return ZYFA_ERR_ALIGN;
+  const int sms = current_device_sms();
+  if (sms <= 0) return ZYFA_ERR_DEVICE;
+  const int e = zyfa::launch_fp8_quantize(x, n, x_dtype == ZYFA_BF16 ? zyfa::kQuantBF16
+                                                                      : zyfa::kQuantF32,
+                                          x8, descale, static_cast<float*>(workspace), sms,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  return e == 0 ? ZYFA_OK : ZYFA_ERR_LAUNCH;
+}
+
+int zyfa_version(void) { return (1 << 16) | 1; }
 
 }  // extern "C"

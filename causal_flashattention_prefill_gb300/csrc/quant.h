@@ -1,0 +1,18 @@
+// Internal interface of the FP8 quantisation kernels (quant.cu).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace zyfa {
+
+constexpr int kQuantBF16 = 0;          // input element types (ZYFA_BF16, ZYFA_F32)
+constexpr int kQuantF32 = 2;
+constexpr int kQuantMaxPartials = 1024; // CTAs of the max pass = floats of workspace
+
+// Enqueues the two quantisation passes; `partial` holds kQuantMaxPartials
+// floats.  Returns a cudaError_t.
+int launch_fp8_quantize(const void* x, int64_t n, int x_type, void* x8, float* descale,
+                        float* partial, int sms, cudaStream_t stream);
+
+}  // namespace zyfa

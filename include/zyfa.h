@@ -59,7 +59,7 @@ typedef enum {
   ZYFA_ERR_DEVICE_TIMEOUT = -6  /* reported by zyfa_device_status()                  */
 } zyfa_status;
 
-enum { ZYFA_BF16 = 0, ZYFA_FP8_E4M3 = 1 };
+enum { ZYFA_BF16 = 0, ZYFA_FP8_E4M3 = 1, ZYFA_F32 = 2 };
 enum { ZYFA_BSHD = 0, ZYFA_BHSD = 1 };
 
 /*
@@ -120,6 +120,34 @@ ZYFA_API int zyfa_device_status(int* value, int reset);
  */
 enum { ZYFA_OPT_SERIALIZE_PV = 1 };
 ZYFA_API int zyfa_set_option(int option, int value);
+
+/*
+ * Per-tensor FP8 quantisation (the input preparation of the FP8 path; ZYFA
+ * README, "Usage": fp8_quantize returns the e4m3 tensor and one power-of-two
+ * descale per tensor as a GPU scalar; "Kernel design": conversions round to
+ * nearest even).
+ *
+ *   descale = smallest power of two with max|x| / descale <= 448 (1 if x is
+ *             all zero);   x8[i] = e4m3(x[i] / descale), ties to even,
+ *             saturating to +-448.
+ *
+ * x          device, n elements of x_dtype (ZYFA_BF16 or ZYFA_F32), 16-byte
+ *            aligned; NaN inputs give unspecified results.
+ * n          element count (>= 0).
+ * x8         device, n bytes of e4m3 codes, 8-byte aligned.
+ * descale    device, one FP32, written by the kernel (the host never waits).
+ * workspace  device scratch of zyfa_fp8_quantize_workspace_bytes() bytes,
+ *            4-byte aligned, owned by the caller; its contents need no
+ *            initialisation and are meaningless after the call.  Calls that
+ *            may overlap on the GPU need separate workspaces.
+ * Two kernels are enqueued on `stream`; deterministic (no atomics).
+ * Returns ZYFA_OK or a negative zyfa_status (checks run before any launch).
+ */
+ZYFA_API int zyfa_fp8_quantize(const void* x, long long n, int x_dtype, void* x8, float* descale,
+                               void* workspace, struct CUstream_st* stream);
+
+/* Bytes of workspace zyfa_fp8_quantize needs (a constant). */
+ZYFA_API long long zyfa_fp8_quantize_workspace_bytes(void);
 
 /* ABI version, (major << 16) | minor. */
 ZYFA_API int zyfa_version(void);

@@ -133,3 +133,28 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(zf._lib, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         zf._lib.load(str(tmp_path / "missing.so"))
+
+
+QUANT_CASES = [
+    (dict(x=0), zf.ZYFA_ERR_ARG),
+    (dict(x8=0), zf.ZYFA_ERR_ARG),
+    (dict(descale=0), zf.ZYFA_ERR_ARG),
+    (dict(ws=0), zf.ZYFA_ERR_ARG),
+    (dict(n=-1), zf.ZYFA_ERR_ARG),
+    (dict(dt=zf.ZYFA_FP8_E4M3), zf.ZYFA_ERR_UNSUPPORTED),
+    (dict(dt=7), zf.ZYFA_ERR_UNSUPPORTED),
+    (dict(x=A + 8), zf.ZYFA_ERR_ALIGN),
+    (dict(x8=A + 4), zf.ZYFA_ERR_ALIGN),
+    (dict(descale=A + 2), zf.ZYFA_ERR_ALIGN),
+]
+
+
+@pytest.mark.parametrize("kw,expected", QUANT_CASES, ids=[str(c[0]) for c in QUANT_CASES])
+def test_quantize_rejects_before_any_cuda_call(lib, kw, expected):
+    a = dict(x=A, n=1024, dt=zf.ZYFA_BF16, x8=A, descale=A, ws=A)
+    a.update(kw)
+    assert zf.zyfa_fp8_quantize(a["x"], a["n"], a["dt"], a["x8"], a["descale"], a["ws"], 0) == expected
+
+
+def test_quantize_workspace_size(lib):
+    assert zf.zyfa_fp8_quantize_workspace_bytes() == 4096

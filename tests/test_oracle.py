@@ -287,3 +287,46 @@ def test_fp8_inputs_decode_exactly():
         ref = t[name].to(torch.float64).numpy() * t[name + "_descale"]
         ours = e4m3_to_f64(workloads.codes(t[name]), t[name + "_descale"])
         assert np.array_equal(ours, ref)
+
+
+# ------------------------------------------------------------- quantiser
+
+from oracle.quantize import descale_of, e4m3_encode_rne, fp8_quantize_f64  # noqa: E402
+
+
+def test_quantize_encoder_matches_torch():
+    """Round-to-nearest-even e4m3 encoding against torch's float8_e4m3fn cast."""
+    rng = np.random.default_rng(11)
+    y = np.concatenate([
+        rng.standard_normal(20000) * 50.0,
+        rng.uniform(-448, 448, 20000),
+        rng.uniform(-2.0 ** -6, 2.0 ** -6, 20000),        # subnormal range
+        e4m3_to_f64(np.arange(0, 126, dtype=np.uint8)),   # exact values
+    ]).astype(np.float32).astype(np.float64)
+    vals = e4m3_to_f64(np.arange(0, 127, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2.0                   # exact ties
+    y = np.concatenate([y, mids, -mids])
+    ref = torch.from_numpy(y.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(e4m3_encode_rne(y), ref)
+
+
+def test_quantize_ties_and_saturation():
+    assert e4m3_encode_rne(np.array([1.0625]))[0] == 0x38      # tie 1.0 | 1.125 -> even
+    assert e4m3_encode_rne(np.array([1.1875]))[0] == 0x3A      # tie 1.125 | 1.25 -> even
+    assert e4m3_encode_rne(np.array([2.0 ** -10]))[0] == 0x00  # half the smallest subnormal
+    assert e4m3_encode_rne(np.array([1000.0]))[0] == 0x7E      # saturates to 448
+    assert e4m3_encode_rne(np.array([-1000.0]))[0] == 0xFE
+
+
+def test_quantize_descale_rule():
+    assert descale_of(448.0) == 1.0
+    assert descale_of(449.0) == 2.0
+    assert descale_of(224.0) == 0.5
+    assert descale_of(224.00001) == 1.0
+    assert descale_of(0.0) == 1.0
+    assert descale_of(3.0) == 2.0 ** -7          # 3 / 2^-7 = 384 <= 448 < 768
+    x = np.random.default_rng(3).standard_normal(1000) * 7.0
+    codes, d = fp8_quantize_f64(x)
+    assert np.abs(x).max() / d <= 448.0 < 2 * np.abs(x).max() / d
+    back = e4m3_to_f64(codes) * d
+    assert np.all(np.abs(back - x) <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * d))
