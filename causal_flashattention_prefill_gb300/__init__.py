@@ -24,6 +24,7 @@ from ._lib import (  # noqa: F401
     load,
     zyfa_device_status,
     zyfa_fp8_quantize,
+    zyfa_fp8_quantize_noalloc,
     zyfa_fp8_quantize_workspace_bytes,
     zyfa_fwd,
     zyfa_fwd_scaled,

@@ -43,6 +43,7 @@ SIGNATURES = {
     "zyfa_version": (_I, []),
     "zyfa_fp8_quantize": (_I, [_P, ctypes.c_longlong, _I, _P, _P, _P, _P]),
     "zyfa_fp8_quantize_workspace_bytes": (ctypes.c_longlong, []),
+    "zyfa_fp8_quantize_noalloc": (_I, [_P, ctypes.c_longlong, _I, _P, _P, _P]),
 }
 
 _lib = None
@@ -110,3 +111,7 @@ def zyfa_fp8_quantize(x, n, x_dtype, x8, descale, workspace, stream) -> int:
 
 def zyfa_fp8_quantize_workspace_bytes() -> int:
     return load().zyfa_fp8_quantize_workspace_bytes()
+
+
+def zyfa_fp8_quantize_noalloc(x, n, x_dtype, x8, descale, stream) -> int:
+    return load().zyfa_fp8_quantize_noalloc(x, n, x_dtype, x8, descale, stream)

@@ -166,3 +166,57 @@ int launch_fp8_quantize(const void* x, int64_t n, int x_type, void* x8, float* d
 }
 
 }  // namespace zyfa
+
+// ---------------------------------------------------------------------------
+// Variant without a caller workspace, for callers that cannot allocate device
+// memory: the per-CTA maxima of the first pass go to a file-scope array
+// instead.  Every device that loads this library keeps these 4 KB until the
+// process exits, and every call on a device shares them.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace zyfa {
+namespace {
+
+static __device__ __align__(256) float g_noalloc_partials[kQuantMaxPartials];
+
+constexpr int kMaxDevicesNoAlloc = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevicesNoAlloc] = {};
+
+}  // namespace
+
+int fp8_quantize_noalloc(const void* x, int64_t n, int x_type, void* x8, float* descale, int sms,
+                         cudaStream_t stream, int* too_large) {
+  *too_large = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevicesNoAlloc) return cudaErrorInvalidDevice;
+  float* partials = nullptr;
+  {
+    // One-time set-up per device, with that device current: host code needs
+    // the array's device address (its name is only a host-side stand-in).
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_partials);
+      if (e != cudaSuccess) return e;
+      g_noalloc_ptr[dev] = static_cast<float*>(p);
+    }
+    partials = g_noalloc_ptr[dev];
+  }
+  // The first pass writes one maximum per CTA and launches at most
+  // min(kQuantMaxPartials, 4 * SMs) CTAs; reject a device whose first pass
+  // would need more slots than the array holds.
+  const int slots = kQuantMaxPartials < 4 * sms ? kQuantMaxPartials : 4 * sms;
+  if (slots > static_cast<int>(sizeof(g_noalloc_partials) / sizeof(float))) {
+    *too_large = 1;
+    return cudaErrorInvalidValue;
+  }
+  // Nothing needs clearing: the second pass reads only the slots the first
+  // pass of the same call has written.
+  return launch_fp8_quantize(x, n, x_type, x8, descale, partials, sms, stream);
+}
+
+}  // namespace zyfa

@@ -15,4 +15,10 @@ constexpr int kQuantMaxPartials = 1024; // CTAs of the max pass = floats of work
 int launch_fp8_quantize(const void* x, int64_t n, int x_type, void* x8, float* descale,
                         float* partial, int sms, cudaStream_t stream);
 
+// Same, with the first pass's maxima in a file-scope device array instead of a
+// caller workspace (one-time symbol lookup per device on first use).  Sets
+// *too_large when the array cannot hold the first pass's maxima.
+int fp8_quantize_noalloc(const void* x, int64_t n, int x_type, void* x8, float* descale, int sms,
+                         cudaStream_t stream, int* too_large);
+
 }  // namespace zyfa

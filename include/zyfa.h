@@ -149,6 +149,30 @@ ZYFA_API int zyfa_fp8_quantize(const void* x, long long n, int x_dtype, void* x8
 /* Bytes of workspace zyfa_fp8_quantize needs (a constant). */
 ZYFA_API long long zyfa_fp8_quantize_workspace_bytes(void);
 
+/*
+ * zyfa_fp8_quantize without a workspace argument, for callers that cannot
+ * allocate device memory: code that only receives the buffers a host
+ * framework planned for it (a fixed memory arena, a plugin interface that
+ * hands over inputs and outputs only), or that runs where an allocation
+ * would stall the device.  The pages have no counterpart to this entry
+ * point; it is a deployment convenience.
+ *
+ * Same arguments, results and errors as zyfa_fp8_quantize, minus
+ * `workspace`.  The scratch it needs (one FP32 maximum per CTA of the first
+ * pass, at most 1024 of them) lives in a 4 KB array inside this library,
+ * kept on every device that runs this entry point until the process exits.
+ * A request whose first pass would need more than those 1024 slots is
+ * rejected with ZYFA_ERR_UNSUPPORTED (this device's first pass uses at most
+ * four per SM).  Nothing in the array has to start at zero, but all calls on
+ * a device share it, so calls that may run at the same time on the GPU (on
+ * different streams without ordering) race and must not be made.  The first
+ * call on each device looks up the array's device address (a CUDA runtime
+ * call) and should come before any stream capture.  The entry point never
+ * allocates: no cudaMalloc, no cudaFree, no allocating library routine.
+ */
+ZYFA_API int zyfa_fp8_quantize_noalloc(const void* x, long long n, int x_dtype, void* x8,
+                                       float* descale, struct CUstream_st* stream);
+
 /* ABI version, (major << 16) | minor. */
 ZYFA_API int zyfa_version(void);
 
