@@ -95,8 +95,8 @@ struct Cfg {
   static constexpr uint32_t kIdescPV = ptx::instr_desc(kFmt, kFmt, 1, kBM, kDV);
   // Register split: the MMA issuer of the d_qk = 192 BF16 form unrolls 12
   // K steps and needs more registers than the others.
-  static constexpr int kSoftmaxRegs = (!kF8 && DQK == 192) ? 192 : 200;
-  static constexpr int kOtherRegs = (!kF8 && DQK == 192) ? 120 : 104;
+  static constexpr int kSoftmaxRegs = (!kF8 && DQK == 192) ? 184 : 200;
+  static constexpr int kOtherRegs = (!kF8 && DQK == 192) ? 136 : 104;
   static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
   static_assert(kNumSlots >= 2, "K/V ring needs at least two slots");
@@ -397,6 +397,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t q_par = 0;   // bit s: parity of the uses of Q buffer s so far
       uint32_t q_used = 0;  // bit s: Q buffer s was loaded at least once
       uint32_t t = 0;       // K/V tiles issued so far (ring position)
+      // The MMA issuer consumes the tiles in units: K_0 alone, then
+      // (V_j, K_j+1) in step j.  Each unit completes on the full barrier of
+      // its first slot (armed with the bytes of the whole unit), so the
+      // issuer waits once per step.  fpar bit x: phase parity of slot x's
+      // full barrier after its last arming; armed bit x: armed at least once.
+      uint32_t fpar = 0, armed = 0;
+      uint32_t unit_bar = 0;
       const int group = p.H / p.Hkv;
       bool ok = true;
       for (int r = 0; ok; ++r) {
@@ -425,16 +432,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = ptx::mbar_wait(bar(B::kSlotEmpty + slot), ((t / NS) & 1u) ^ 1u, abort, status,
                                 1);
             if (!ok) break;
-            const uint32_t fb = bar(B::kSlotFull + slot);
             const uint32_t dst = slots_smem + slot * C::kSlotBytes;
             if (kv == 0) {
-              ptx::mbar_arrive_expect_tx(fb, C::kTileBytesQK);
+              uint32_t fb = unit_bar;  // K_j, j > 0: second tile of the unit (V_j-1, K_j)
+              if (j == 0) {
+                fb = bar(B::kSlotFull + slot);
+                ptx::mbar_arrive_expect_tx(fb, C::kTileBytesQK);
+                fpar ^= 1u << slot;
+                armed |= 1u << slot;
+              }
 #pragma unroll
               for (int c = 0; c < C::kChunksQK; ++c)
                 tma_tile(&tm_k, dst + c * C::kChunkBytesQK, fb, p.layout,
                          c * C::kChunkElemsQK, hk, j * kBN, it.b, pol_kv);
             } else {
-              ptx::mbar_arrive_expect_tx(fb, C::kTileBytesV);
+              const uint32_t fb = bar(B::kSlotFull + slot);
+              ptx::mbar_arrive_expect_tx(
+                  fb, C::kTileBytesV + (j + 1 < it.nload ? C::kTileBytesQK : 0));
+              fpar ^= 1u << slot;
+              armed |= 1u << slot;
+              unit_bar = fb;
 #pragma unroll
               for (int c = 0; c < C::kChunksV; ++c)
                 tma_tile(&tm_v, dst + c * C::kChunkBytesV, fb, p.layout, c * C::kChunkElemsV,
@@ -446,11 +463,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) {
         // Unwind: let every copy this thread issued land before the CTA's
-        // shared memory is released.
-        for (uint32_t i = 0; i < NS && i < t; ++i) {
-          const uint32_t last = t - 1 - i;  // the last use of slot last % NS
-          ptx::mbar_drain(bar(B::kSlotFull + last % NS), (last / NS) & 1u);
-        }
+        // shared memory is released (each copy completes on the last
+        // arming of some slot's full barrier).
+        for (int x = 0; x < NS; ++x)
+          if ((armed >> x) & 1u) ptx::mbar_drain(bar(B::kSlotFull + x), ((fpar >> x) & 1u) ^ 1u);
         for (int s = 0; s < 2; ++s)
           if ((q_used >> s) & 1u) ptx::mbar_drain(bar(B::kQFull + s), ((q_par >> s) & 1u) ^ 1u);
       }
@@ -462,6 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t q_par = 0, p_par = 0, pv_par = 0;  // bit s: phase parity per stage
       uint32_t p_count[2] = {0u, 0u};             // P tiles received per stage
       uint32_t t = 0;
+      uint32_t fpar = 0;  // bit x: phase parity of slot x's full barrier to wait for next
       bool ok = true;
       // Base descriptors; an MMA adds its byte offset >> 4 to the start
       // address field (addresses stay below 256 KB, so no carry leaves it).
@@ -507,8 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         // Prologue: S of K/V tile 0 for both stages.
         uint32_t slot_k = t % NS;
-        ok = ptx::mbar_wait(bar(B::kSlotFull + slot_k), (t / NS) & 1u, abort, status, 1);
+        ok = ptx::mbar_wait(bar(B::kSlotFull + slot_k), (fpar >> slot_k) & 1u, abort, status, 1);
         if (!ok) break;
+        fpar ^= 1u << slot_k;
         ++t;
         ptx::tc_fence_after();
         issue_s(0, slot_k);
@@ -520,19 +538,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(bar(B::kSlotEmpty + slot_k));
 
         for (int j = 0; j < it.nload && ok; ++j) {
+          // One wait covers V_j and (when there is a next tile) K_j+1.
           const uint32_t slot_v = t % NS;
-          const uint32_t par_v = (t / NS) & 1u;
           ++t;
           const bool has_next = j + 1 < it.nload;
-          uint32_t par_k = 0;
           if (has_next) {
             slot_k = t % NS;
-            par_k = (t / NS) & 1u;
             ++t;
           }
-          bool k_ready = false;
-          ok = ptx::mbar_wait(bar(B::kSlotFull + slot_v), par_v, abort, status, 1);
+          ok = ptx::mbar_wait(bar(B::kSlotFull + slot_v), (fpar >> slot_v) & 1u, abort, status, 1);
           if (!ok) break;
+          fpar ^= 1u << slot_v;
           for (int s = 0; s < 2; ++s) {
             const int ns = s == 0 ? it.n0 : it.n1;
             if (j >= ns) continue;
@@ -541,8 +557,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             p_par ^= 1u << s;
             ++p_count[s];
             ptx::tc_fence_after();
+            // The flag is read before the MMAs are issued and used after
+            // them: a shared-memory load from this thread takes hundreds of
+            // cycles while the tensor core streams its operands, and the
+            // MMA queue would run dry if the issue waited for it.
+            uint32_t lo_flag = 0;
+            if constexpr (C::kF8) lo_flag = sm.pflag[s];
             issue_pv(s, slot_v, j > 0, 0);
-            if (C::kF8 && sm.pflag[s] == p_count[s]) issue_pv(s, slot_v, true, 32);  // lo term
+            if (C::kF8 && lo_flag == p_count[s]) issue_pv(s, slot_v, true, 32);  // lo term
             if (p.serialize_pv && j + 1 < ns) {
               // Verification mode: P (aliasing S) is fully consumed before the
               // next S MMA of this stage overwrites it.
@@ -552,12 +574,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ok) break;
             }
             if (j + 1 < ns) {
-              if (!k_ready) {
-                ok = ptx::mbar_wait(bar(B::kSlotFull + slot_k), par_k, abort, status, 1);
-                if (!ok) break;
-                ptx::tc_fence_after();
-                k_ready = true;
-              }
               issue_s(s, slot_k);
               ptx::mma_commit(bar(B::kSFull + s));
             } else {
