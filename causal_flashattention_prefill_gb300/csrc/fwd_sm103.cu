@@ -90,6 +90,12 @@ struct Cfg {
   // FP8 P is stored as e4m3 of p * 2^4 (p <= 2^tau keeps it below 448); the
   // factor enters as +4 in the exponent.
   static constexpr float kPLog2Scale = kF8 ? 4.0f : 0.0f;
+  // Largest p that needs no rescale: 2^(tau + pre-scale).
+  static constexpr float kPCap = 256.0f;
+  static_assert(kTau + kPLog2Scale == 8.0f, "kPCap is 2^(tau + pre-scale)");
+  // Accuracy test: a p above 1/kAccRatio of the row's mass so far takes the
+  // exact path (BF16 rounded-sum denominator, FP8 two-term P).
+  static constexpr float kAccRatio = kF8 ? 32.0f : 8.0f;
   static constexpr uint32_t kFmt = kF8 ? 0u : 1u;   // E4M3 / BF16
   static constexpr uint32_t kIdescQK = ptx::instr_desc(kFmt, kFmt, 0, kBM, kBN);
   static constexpr uint32_t kIdescPV = ptx::instr_desc(kFmt, kFmt, 1, kBM, kDV);
@@ -167,11 +173,15 @@ __device__ __forceinline__ void tma_tile(const CUtensorMap* m, uint32_t dst, uin
     ptx::tma_load_4d(dst, m, bar, c0, row, head, b, pol);
 }
 
-// One lane polls, the verdict is broadcast: the warp leaves the wait
+// Waits for a phase with the whole warp: the warp leaves the wait
 // converged and in agreement, as the .sync.aligned tcgen05 instructions that
 // follow require.
 __device__ __forceinline__ bool warp_wait(uint32_t b, uint32_t parity, volatile int* abort,
                                           int* status, int lane) {
+  // Common case: every lane sees the completed phase (one vote, no
+  // divergence).  Otherwise one lane waits with the timeout and the verdict
+  // is broadcast.
+  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(b, parity))) return true;
   int ok = 0;
   if (lane == 0) ok = ptx::mbar_wait(b, parity, abort, status, 1) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -203,10 +213,13 @@ __device__ __forceinline__ float row_max128(const float* f) {
 // residual at column offset 32), stored to tensor memory over S.  `sacc`
 // accumulates the unrounded sum; with kExact (BF16) `rr` accumulates the sum
 // of the rounded values that multiply V.
-template <class C, bool kExact>
+// kTest (FP8): every packed word of P also enters the threshold test
+// tacc |= word + tk (see threshold_addend).
+template <class C, bool kExact, bool kTest = false>
 __device__ __forceinline__ void produce_half(const float* f, float c_log2, float neg_m,
                                              uint32_t t_s, int h, bool two_term,
-                                             float2 (&sacc)[2], float& rr) {
+                                             float2 (&sacc)[2], float& rr, uint32_t tk = 0,
+                                             uint32_t* tacc = nullptr) {
   const float2 c2 = make_float2(c_log2, c_log2);
   const float2 nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
@@ -226,6 +239,10 @@ __device__ __forceinline__ void produce_half(const float* f, float c_log2, float
       for (int i = 0; i < 8; ++i)
         pk[i] = ptx::pack_e4m3x4(e[4 * i], e[4 * i + 1], e[4 * i + 2], e[4 * i + 3]);
       ptx::tmem_st8(t_s + ch * 8, pk);
+      if constexpr (kTest) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) *tacc |= pk[i] + tk;
+      }
       if (two_term) {
         uint32_t lo[8];
 #pragma unroll
@@ -250,6 +267,14 @@ __device__ __forceinline__ void produce_half(const float* f, float c_log2, float
       }
     }
   }
+}
+
+// FP8 threshold test on packed P.  The e4m3 code of a non-negative value is
+// monotonic in the value and at most 0x7E, so adding 0x80 - c to every byte
+// of a word sets that byte's top bit exactly when its code is >= c, without
+// carries between bytes.  Returns the per-byte addend for code c.
+__device__ __forceinline__ uint32_t threshold_addend(uint32_t c) {
+  return (0x80u - c) * 0x01010101u;
 }
 
 // FP8: the e4m3 rounding residual of P (lo term) for the 128 scores of the
@@ -671,19 +696,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           // tau is recomputed after the rescale (rare: tau is large).
           float neg_m = C::kPLog2Scale - m_ref;
           float2 sacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-          const float m_lo = row_max64(f);
-          produce_half<C, false>(f, c_log2, neg_m, t_s, 0, false, sacc, rr);
+          // FP8: the tests run on the packed P (threshold_addend): a code at
+          // or above that of min(kPCap, l / kAccRatio) sends the warp to the
+          // exact path.  Both tests are then conservative: p > kPCap or
+          // p * kAccRatio > l + rs implies such a code (rounding to e4m3 is
+          // monotonic and l <= l + rs).
+          uint32_t tk = 0, tacc = 0;
+          if constexpr (C::kF8) {
+            const uint32_t cap_code = ptx::pack_e4m3x4(C::kPCap, 0.f, 0.f, 0.f) & 0xFFu;
+            const uint32_t acc_code = ptx::pack_e4m3x4(l * (1.0f / C::kAccRatio), 0.f, 0.f, 0.f) & 0xFFu;
+            tk = threshold_addend(acc_code < cap_code ? acc_code : cap_code);
+          }
+          produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 0, false, sacc, rr, tk, &tacc);
           ptx::tmem_wait_ld_dep64(*reinterpret_cast<uint32_t(*)[64]>(&v[64]));
           if (diag) {
 #pragma unroll
             for (int c = 64; c < 128; ++c)
               if (c > row_in_tile) f[c] = -INFINITY;
           }
-          const float m_hi = row_max64(f + 64);
-          produce_half<C, false>(f, c_log2, neg_m, t_s, 1, false, sacc, rr);
+          produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 1, false, sacc, rr, tk, &tacc);
           const float2 t2 = __fadd2_rn(sacc[0], sacc[1]);
           rs = t2.x + t2.y;
-          const float mx = fmaxf(m_lo, m_hi) * c_log2;
+          // The unrounded sum bounds every p of the tile (all p >= 0).  When
+          // it is small enough, neither the rescale test nor the accuracy
+          // test can fire and the tile maximum is not needed (the 0.1%
+          // margin covers the rounding of exp2 and of the sum); otherwise
+          // the warp forms the maximum and takes the tests exactly.
+          const float bound = rs * 1.001f;
+          const bool quiet = C::kF8 ? (tacc & 0x80808080u) == 0u
+                                    : (bound <= C::kPCap && bound * C::kAccRatio <= l + rs);
+          if ((C::kF8 && diag) || !__all_sync(0xffffffffu, quiet)) {
+          const float mx = row_max128(f) * c_log2;
           const bool need = mx > m_ref + C::kTau;
           if (__any_sync(0xffffffffu, need)) {
             const float alpha = need ? ptx::ex2(m_ref - mx) : 1.0f;
@@ -715,6 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             exact = __any_sync(0xffffffffu, p_max * 8.0f > l + rs);
             if (exact) rr = rounded_sum_bf16(f, c_log2, neg_m);
+          }
           }
         }
         if (C::kF8) {
