@@ -269,38 +269,49 @@ def e2e_measure(w, t, steps, device):
 # ------------------------------------------------------------ CPU oracle
 
 def oracle_sample(w, budget_s: float = 15.0, t=None):
-    """Times the float64 oracle on a bounded sample of the workload: the last
-    rows of the sequence (the longest causal rows) of successive (b, h) slices,
-    growing the sample until about ``budget_s`` seconds of CPU work."""
+    """Times the float64 oracle on a bounded sample of the workload: 256-row
+    blocks of query rows taken from the end of the sequence backwards (the
+    longest causal rows first), each over every (batch, head) slice in turn,
+    until about ``budget_s`` seconds of CPU work have been spent."""
     import oracle
     if t is None:
         t = workloads.make_inputs(w)
     q, k, v = (workloads.codes(t[n]) for n in ("q", "k", "v"))
     group = w.H // w.Hkv
     R = min(w.S, 256)
-    rows = np.arange(w.S - R, w.S)
-    flops_per_head = float(sum(2.0 * (i + 1) * (w.d_qk + w.d_v) for i in rows))
+    n_blocks = (w.S + R - 1) // R
     elapsed = 0.0
-    heads_done = 0
-    while elapsed < budget_s and heads_done < w.B * w.H:
-        b, h = divmod(heads_done, w.H)
-        hk = h // group
-        if w.layout == "bshd":
-            qs, ks, vs = q[b:b + 1, :, h:h + 1], k[b:b + 1, :, hk:hk + 1], v[b:b + 1, :, hk:hk + 1]
-        else:
-            qs, ks, vs = q[b:b + 1, h:h + 1], k[b:b + 1, hk:hk + 1], v[b:b + 1, hk:hk + 1]
-        t0 = time.perf_counter()
-        oracle.attention_rows_f64(qs, ks, vs, rows, dtype=w.dtype, layout=w.layout,
-                                  q_descale=t["q_descale"], k_descale=t["k_descale"],
-                                  v_descale=t["v_descale"])
-        elapsed += time.perf_counter() - t0
-        heads_done += 1
-    flops = flops_per_head * heads_done
+    flops = 0.0
+    slices = 0
+    blocks_used = 0
+    for blk in range(n_blocks):
+        hi = w.S - blk * R
+        rows = np.arange(max(0, hi - R), hi)
+        block_flops = float(sum(2.0 * (i + 1) * (w.d_qk + w.d_v) for i in rows))
+        blocks_used = blk + 1
+        for bh in range(w.B * w.H):
+            if elapsed >= budget_s:
+                break
+            b, h = divmod(bh, w.H)
+            hk = h // group
+            if w.layout == "bshd":
+                qs, ks, vs = q[b:b + 1, :, h:h + 1], k[b:b + 1, :, hk:hk + 1], v[b:b + 1, :, hk:hk + 1]
+            else:
+                qs, ks, vs = q[b:b + 1, h:h + 1], k[b:b + 1, hk:hk + 1], v[b:b + 1, hk:hk + 1]
+            t0 = time.perf_counter()
+            oracle.attention_rows_f64(qs, ks, vs, rows, dtype=w.dtype, layout=w.layout,
+                                      q_descale=t["q_descale"], k_descale=t["k_descale"],
+                                      v_descale=t["v_descale"])
+            elapsed += time.perf_counter() - t0
+            flops += block_flops
+            slices += 1
+        if elapsed >= budget_s:
+            break
     cores = len(os.sched_getaffinity(0))
     return {"value": flops / elapsed / 1e12, "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle", "seconds": elapsed,
-            "sample": f"rows {w.S - R}..{w.S - 1} of {heads_done} (batch, head) slices of "
-                      f"{w.name} (numpy float64, materialised masked scores, "
+            "sample": f"{slices} (batch, head, {R}-row block) slices from the last {blocks_used} "
+                      f"query blocks of {w.name} (numpy float64, materialised masked scores, "
                       f"{cores} host threads available to BLAS)"}
 
 
