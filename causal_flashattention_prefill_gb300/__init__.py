@@ -1,9 +1,10 @@
 """GB300 (sm_103a) causal prefill attention.
 
 ``zyfa_*`` are the C ABI entry points (ctypes, argument marshalling only).
-``flash_attn_func`` and ``fp8_quantize`` are the torch-level conveniences with
-the calling conventions of the ZYFA README ("Usage", "Differences from
-flash-attn"); every step of the attention itself runs in the CUDA library.
+``flash_attn_func`` (with its qkv-packed, kv-packed and equal-length varlen
+forms) and ``fp8_quantize`` are the torch-level conveniences with the calling
+conventions of the ZYFA README ("Usage", "Differences from flash-attn"); every
+step of the attention itself runs in the CUDA library.
 """
 
 from ._lib import (  # noqa: F401
@@ -33,4 +34,12 @@ from ._lib import (  # noqa: F401
     zyfa_validate,
     zyfa_version,
 )
-from .api import ZyfaError, attention, flash_attn_func, fp8_quantize  # noqa: F401
+from .api import (  # noqa: F401
+    ZyfaError,
+    attention,
+    flash_attn_func,
+    flash_attn_kvpacked_func,
+    flash_attn_qkvpacked_func,
+    flash_attn_varlen_func,
+    fp8_quantize,
+)

@@ -1,13 +1,16 @@
 """Torch-level wrappers over the C ABI.
 
 PyTorch supplies device memory and the current stream; the attention runs in
-the CUDA library only.  ``flash_attn_func`` follows the calling conventions
-the ZYFA README lists ("Usage", "Differences from flash-attn").
+the CUDA library only.  ``flash_attn_func`` and its packed and varlen forms
+follow the calling conventions the ZYFA README lists ("Usage", "Differences
+from flash-attn") and reach the library through the custom operator
+``torch.ops.zyfa.fwd``.
 """
 
 from __future__ import annotations
 
 import math
+from typing import Optional, Tuple
 
 import torch
 
@@ -105,16 +108,6 @@ def fp8_quantize(x: torch.Tensor, workspace: torch.Tensor = None, stream=None):
     return x8, descale
 
 
-class _NoBackward(torch.autograd.Function):
-    @staticmethod
-    def forward(ctx, out, *inputs):
-        return out
-
-    @staticmethod
-    def backward(ctx, *grads):
-        raise RuntimeError("causal prefill attention has no backward pass")
-
-
 def _descale_tensor(d, device):
     if d is None:
         return None
@@ -124,6 +117,46 @@ def _descale_tensor(d, device):
         raise TypeError("a descale is a Python float or a float32 tensor")
     # A (B, Hkv) expansion of one value is read through its first element.
     return d.reshape(-1)[:1] if d.numel() > 1 else d.reshape(1)
+
+
+# The attention is registered as the custom operator torch.ops.zyfa.fwd (ZYFA
+# README, "Usage"), so torch.compile traces through calls and they can be
+# captured in CUDA graphs (the library allocates nothing and never waits for
+# the host).  The fake implementation gives torch.compile the output shapes.
+# The LSE output is a (0,)-shaped tensor when it is not requested.
+@torch.library.custom_op("zyfa::fwd", mutates_args=())
+def _fwd_op(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
+            q_descale: Optional[torch.Tensor], k_descale: Optional[torch.Tensor],
+            v_descale: Optional[torch.Tensor], softmax_scale: float, layout: str,
+            return_lse: bool) -> Tuple[torch.Tensor, torch.Tensor]:
+    res = attention(q, k, v, q_descale=q_descale, k_descale=k_descale, v_descale=v_descale,
+                    softmax_scale=softmax_scale, layout=layout, return_lse=return_lse)
+    if return_lse:
+        return res
+    return res, torch.empty(0, dtype=torch.float32, device=q.device)
+
+
+def _out_lse_shapes(q, v, layout):
+    if layout == "bshd":
+        B, S, H, _ = q.shape
+        return (B, S, H, v.shape[3]), (B, H, S)
+    B, H, S, _ = q.shape
+    return (B, H, S, v.shape[3]), (B, H, S)
+
+
+@_fwd_op.register_fake
+def _(q, k, v, q_descale, k_descale, v_descale, softmax_scale, layout, return_lse):
+    o_shape, l_shape = _out_lse_shapes(q, v, layout)
+    out = q.new_empty(o_shape, dtype=torch.bfloat16)
+    lse = q.new_empty(l_shape if return_lse else (0,), dtype=torch.float32)
+    return out, lse
+
+
+def _fwd_backward(ctx, *grads):
+    raise RuntimeError("causal prefill attention has no backward pass")
+
+
+_fwd_op.register_autograd(_fwd_backward)
 
 
 def flash_attn_func(q, k, v, dropout_p=0.0, softmax_scale=None, causal=True,
@@ -142,14 +175,108 @@ def flash_attn_func(q, k, v, dropout_p=0.0, softmax_scale=None, causal=True,
     fp8 = q.dtype == torch.float8_e4m3fn
     if fp8 and (q_descale is None or k_descale is None or v_descale is None):
         raise ValueError("FP8 inputs need q_descale, k_descale and v_descale")
+    if layout not in ("bshd", "bhsd"):
+        raise ValueError(f"layout is 'bshd' or 'bhsd', not {layout!r}")
     q, k, v = (t.contiguous() for t in (q, k, v))
     dq, dk, dv = (_descale_tensor(d, q.device) for d in (q_descale, k_descale, v_descale))
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(q.shape[-1])
+    want_lse = bool(return_lse or return_attn_probs)
+    out, lse = torch.ops.zyfa.fwd(q, k, v, dq, dk, dv, float(softmax_scale), layout, want_lse)
+    if not want_lse:
+        lse = None
+    if return_attn_probs:
+        return out, lse, None
+    if return_lse:
+        return out, lse
+    return out
+
+
+def _check_unsupported(softcap=0.0, alibi_slopes=None, deterministic=False, block_table=None):
+    if softcap not in (0, 0.0, None):
+        raise ValueError("softcap is not supported")
+    if alibi_slopes is not None:
+        raise ValueError("ALiBi is not supported")
+    if block_table is not None:
+        raise ValueError("paged KV is not supported")
+    # Every result is deterministic, so `deterministic` needs no action.
+
+
+def flash_attn_qkvpacked_func(qkv, dropout_p=0.0, softmax_scale=None, causal=True,
+                              window_size=(-1, -1), softcap=0.0, alibi_slopes=None,
+                              deterministic=False, return_attn_probs=False, q_descale=None,
+                              k_descale=None, v_descale=None, return_lse=False):
+    """flash-attn's packed form: ``qkv`` is (batch, seqlen, 3, nheads, headdim)
+    (MHA, d_qk = d_v).  The three slices are copied to contiguous tensors
+    before the kernel runs (ZYFA README, "Differences from flash-attn")."""
+    _check_unsupported(softcap, alibi_slopes, deterministic)
+    if qkv.dim() != 5 or qkv.shape[2] != 3:
+        raise ValueError("qkv must be (batch, seqlen, 3, nheads, headdim)")
+    q, k, v = qkv.unbind(dim=2)
+    return flash_attn_func(q, k, v, dropout_p, softmax_scale, causal, window_size,
+                           q_descale=q_descale, k_descale=k_descale, v_descale=v_descale,
+                           return_lse=return_lse, return_attn_probs=return_attn_probs)
+
+
+def flash_attn_kvpacked_func(q, kv, dropout_p=0.0, softmax_scale=None, causal=True,
+                             window_size=(-1, -1), softcap=0.0, alibi_slopes=None,
+                             deterministic=False, return_attn_probs=False, q_descale=None,
+                             k_descale=None, v_descale=None, return_lse=False):
+    """flash-attn's packed-KV form: ``q`` (batch, seqlen, nheads, headdim),
+    ``kv`` (batch, seqlen, 2, nheads_k, headdim) (d_qk = d_v)."""
+    _check_unsupported(softcap, alibi_slopes, deterministic)
+    if kv.dim() != 5 or kv.shape[2] != 2:
+        raise ValueError("kv must be (batch, seqlen, 2, nheads_k, headdim)")
+    k, v = kv.unbind(dim=2)
+    return flash_attn_func(q, k, v, dropout_p, softmax_scale, causal, window_size,
+                           q_descale=q_descale, k_descale=k_descale, v_descale=v_descale,
+                           return_lse=return_lse, return_attn_probs=return_attn_probs)
+
+
+def _equal_segments(cu_seqlens, max_seqlen, total, name):
+    """Batch size of an equal-length varlen batch; checks the metadata that can
+    be checked without waiting for the device."""
+    if max_seqlen <= 0 or total % max_seqlen != 0:
+        raise ValueError(f"{name}: sequences must all have length max_seqlen "
+                         f"({total} tokens, max_seqlen {max_seqlen})")
+    batch = total // max_seqlen
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() != batch + 1:
+        raise ValueError(f"{name}: cu_seqlens must hold batch + 1 = {batch + 1} offsets")
+    if cu_seqlens.device.type == "cpu":
+        want = torch.arange(0, total + 1, max_seqlen, dtype=cu_seqlens.dtype)
+        if not torch.equal(cu_seqlens, want):
+            raise ValueError(f"{name}: only sequences of equal length are supported")
+    return batch
+
+
+def flash_attn_varlen_func(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+                           dropout_p=0.0, softmax_scale=None, causal=True, window_size=(-1, -1),
+                           softcap=0.0, alibi_slopes=None, deterministic=False,
+                           return_attn_probs=False, block_table=None, q_descale=None,
+                           k_descale=None, v_descale=None, return_lse=False):
+    """flash-attn's varlen form for batches of equal-length sequences (ZYFA
+    README, "Usage"): ``q`` (total, nheads, headdim), ``k``/``v`` (total,
+    nheads_k, headdim), ``cu_seqlens_*`` = [0, S, 2S, ...].  Device-resident
+    offsets are trusted (checking them would wait for the device); offsets on
+    the host are checked.  Returns ``out`` (total, nheads, d_v) and, on
+    request, the LSE as (nheads, total)."""
+    _check_unsupported(softcap, alibi_slopes, deterministic, block_table)
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("varlen q, k, v are (total_tokens, heads, headdim)")
+    if max_seqlen_q != max_seqlen_k or q.shape[0] != k.shape[0] or k.shape[0] != v.shape[0]:
+        raise ValueError("causal prefill needs seqlen_q = seqlen_k for every sequence")
+    batch = _equal_segments(cu_seqlens_q, max_seqlen_q, q.shape[0], "cu_seqlens_q")
+    _equal_segments(cu_seqlens_k, max_seqlen_k, k.shape[0], "cu_seqlens_k")
+    S = max_seqlen_q
+    q4, k4, v4 = (t.reshape(batch, S, t.shape[1], t.shape[2]) for t in (q, k, v))
     want_lse = return_lse or return_attn_probs
-    res = attention(q, k, v, q_descale=dq, k_descale=dk, v_descale=dv,
-                    softmax_scale=softmax_scale, layout=layout, return_lse=want_lse)
+    res = flash_attn_func(q4, k4, v4, dropout_p, softmax_scale, causal, window_size,
+                          q_descale=q_descale, k_descale=k_descale, v_descale=v_descale,
+                          return_lse=want_lse)
     out, lse = res if want_lse else (res, None)
-    if torch.is_grad_enabled() and any(t.requires_grad for t in (q, k, v)):
-        out = _NoBackward.apply(out, q, k, v)
+    out = out.reshape(batch * S, out.shape[2], out.shape[3])
+    if lse is not None:
+        lse = lse.permute(1, 0, 2).reshape(lse.shape[1], batch * S)
     if return_attn_probs:
         return out, lse, None
     if return_lse:
