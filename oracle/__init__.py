@@ -18,3 +18,10 @@ from .attention import (  # noqa: F401
     decode_inputs_f64,
 )
 from .formats import bf16_to_f64, e4m3_to_f64  # noqa: F401
+from .rotation import (  # noqa: F401
+    dct3_f64,
+    fp8_quantize_rotated_f64,
+    hadamard_f64,
+    rotate_f64,
+    rotation_f64,
+)

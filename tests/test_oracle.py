@@ -330,3 +330,119 @@ def test_quantize_descale_rule():
     assert np.abs(x).max() / d <= 448.0 < 2 * np.abs(x).max() / d
     back = e4m3_to_f64(codes) * d
     assert np.all(np.abs(back - x) <= np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * d))
+
+
+# ------------------------------------------------------------- rotation
+
+import oracle.rotation as orot  # noqa: E402
+
+
+def _signs(d, seed):
+    return np.where(np.random.default_rng(seed).integers(0, 2, d) == 1, 1.0, -1.0)
+
+
+def rpin_hadamard_small_cases():
+    """Sylvester's construction: H_2 and H_4 written out, H H^T = n I."""
+    assert np.array_equal(orot.hadamard_f64(1), [[1.0]])
+    assert np.array_equal(orot.hadamard_f64(2), [[1, 1], [1, -1]])
+    assert np.array_equal(orot.hadamard_f64(4), [[1, 1, 1, 1], [1, -1, 1, -1],
+                                                 [1, 1, -1, -1], [1, -1, -1, 1]])
+    for n in (8, 64, 128):
+        h = orot.hadamard_f64(n)
+        assert np.all(np.abs(h) == 1.0)
+        assert np.array_equal(h @ h.T, n * np.eye(n))
+
+
+def rpin_dct3_closed_form():
+    """Orthonormal DCT-II of size 3: rows [1,1,1]/sqrt3, [1,0,-1]/sqrt2, [1,-2,1]/sqrt6."""
+    c = orot.dct3_f64()
+    want = np.array([[1, 1, 1] / np.sqrt(3), [1, 0, -1] / np.sqrt(2), [1, -2, 1] / np.sqrt(6)])
+    np.testing.assert_allclose(c, want, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(c @ c.T, np.eye(3), rtol=0, atol=1e-15)
+
+
+def rpin_orthogonal_and_products_kept():
+    """R R^T = I, and (qR)(kR)^T = q k^T: the scores are unchanged."""
+    for d in (128, 192):
+        s = _signs(d, d)
+        r = orot.rotation_f64(d, s)
+        np.testing.assert_allclose(r @ r.T, np.eye(d), rtol=0, atol=1e-13)
+        q, k = _rand((40, d), 1), _rand((50, d), 2)
+        np.testing.assert_allclose(orot.rotate_f64(q, s) @ orot.rotate_f64(k, s).T, q @ k.T,
+                                   rtol=0, atol=1e-11)
+
+
+def rpin_elementwise_definition():
+    """Every entry from its definition by plain loops: d=128 R[i,j] =
+    s_i H[i,j] / sqrt(128) with H[i,j] = (-1)^popcount(i & j) (the closed
+    form of Sylvester's matrix); d=192 R[64a+b, 64c+e] = s_(64a+b) *
+    C3[c,a] * (-1)^popcount(b & e) / 8."""
+    s = _signs(128, 5)
+    r = orot.rotation_f64(128, s)
+    for i in range(0, 128, 7):
+        for j in range(128):
+            want = s[i] * (-1.0) ** bin(i & j).count("1") / math.sqrt(128)
+            assert abs(r[i, j] - want) < 1e-15
+    s = _signs(192, 6)
+    r = orot.rotation_f64(192, s)
+    c3 = orot.dct3_f64()
+    for a in range(3):
+        for b in range(0, 64, 5):
+            for cc in range(3):
+                for e in range(64):
+                    want = s[64 * a + b] * c3[cc, a] * (-1.0) ** bin(b & e).count("1") / 8.0
+                    assert abs(r[64 * a + b, 64 * cc + e] - want) < 1e-15
+
+
+def rpin_unit_vectors():
+    """x = e_i gives row i of R, and rotating a quantised tensor is the
+    quantisation of x @ R."""
+    s = _signs(128, 7)
+    r = orot.rotation_f64(128, s)
+    np.testing.assert_array_equal(orot.rotate_f64(np.eye(128)[[3, 77]], s), r[[3, 77]])
+    x = _rand((9, 128), 8) * 30.0
+    codes, d = orot.fp8_quantize_rotated_f64(x, s)
+    c2, d2 = fp8_quantize_f64(x @ r)
+    assert d == d2 and np.array_equal(codes, c2)
+
+
+RPINS = [rpin_hadamard_small_cases, rpin_dct3_closed_form, rpin_orthogonal_and_products_kept,
+         rpin_elementwise_definition, rpin_unit_vectors]
+
+
+@pytest.mark.parametrize("pin", RPINS, ids=lambda p: p.__name__)
+def test_rotation_pin(pin):
+    pin()
+
+
+_orig_hadamard = orot.hadamard_f64
+_orig_dct3 = orot.dct3_f64
+
+ROT_MUTANTS = {
+    # H_2n built as [[H, H], [-H, H]] (a plausible sign slip)
+    "hadamard_sign_slip": ("hadamard_f64", lambda n: (lambda h: np.block(
+        [[h, h], [-h, h]]))(_orig_hadamard(n // 2)) if n > 1 else _orig_hadamard(n)),
+    "dct_transposed": ("dct3_f64", lambda: _orig_dct3().T),
+    "dct_unnormalised": ("dct3_f64", lambda: _orig_dct3() * math.sqrt(3 / 2)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ROT_MUTANTS))
+def test_rotation_mutants_are_caught(name, monkeypatch):
+    attr, fn = ROT_MUTANTS[name]
+    monkeypatch.setattr(orot, attr, fn)
+    caught = []
+    for pin in RPINS:
+        try:
+            pin()
+        except AssertionError:
+            caught.append(pin.__name__)
+    assert caught, f"planted mistake {name} passed every rotation pin"
+
+
+def test_rotation_mutant_signs_dropped(monkeypatch):
+    """Signs ignored: the element-wise pin catches it."""
+    orig = orot.rotation_f64
+    monkeypatch.setattr(orot, "rotation_f64", lambda d, s: orig(d, np.ones(d)))
+    with pytest.raises(AssertionError):
+        rpin_elementwise_definition()
