@@ -194,6 +194,51 @@ def run_timed(launch, flush, starts, ends, device):
     return [s.elapsed_time(e) for s, e in zip(starts, ends)], wall
 
 
+def time_rotate_quantize(w, steps, warmup, device, peaks, peak_src):
+    """The FP8 input step with rotation (rotate + quantise q of the workload
+    through zyfa_fp8_quantize_rotated), timed like the attention kernel.  HBM
+    bound: the algorithmic bytes are one read of x and one write of the codes
+    (3 bytes per BF16 element); the kernel reads x twice (max pass, then
+    quantise pass)."""
+    import torch
+    import causal_flashattention_prefill_gb300 as zf
+
+    t = workloads.make_inputs(w)
+    x = t["q"].to(device)                         # BF16 (B, S, H, d)
+    d = x.shape[-1]
+    rows = x.numel() // d
+    signs = zf.hadamard_signs(d, seed=0, device=device)
+    x8 = torch.empty(x.shape, dtype=torch.uint8, device=device)
+    ds = torch.empty(1, dtype=torch.float32, device=device)
+    ws = torch.empty(zf.zyfa_fp8_quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device).cuda_stream
+
+    def launch():
+        st = zf.zyfa_fp8_quantize_rotated(x.data_ptr(), rows, d, zf.ZYFA_BF16, signs.data_ptr(),
+                                          x8.data_ptr(), ds.data_ptr(), ws.data_ptr(), stream)
+        if st != zf.ZYFA_OK:
+            raise zf.ZyfaError(st)
+
+    for _ in range(warmup):
+        flush.zero_()
+        launch()
+    torch.cuda.synchronize(device)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ms, _ = run_timed(launch, flush, starts, ends, device)
+    mean_ms = statistics.mean(ms)
+    algo_bytes = 3.0 * x.numel()
+    gbs = algo_bytes / (mean_ms * 1e-3) / 1e9
+    hbm = peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    return {"workload": f"fp8_quantize_rotated on q of {w.name} (d={d}, BF16 in)",
+            "value": gbs, "unit": "GB/s", "ms_per_launch": mean_ms, "gpu_launches": 2 * steps,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "traffic": None,
+                         "algorithmic_bytes_per_launch": algo_bytes,
+                         "peak_source": f"{peak_src} copy bandwidth"}}
+
+
 def sampled_parity(w, t, out, lse, n_rows=64):
     """Checks a few rows of the timed launch against the oracle before timing."""
     import oracle
@@ -418,6 +463,9 @@ def main():
                          "ms_per_launch": statistics.mean(ms2), "peak": p2,
                          "frac": v2 / p2, "parity": par2})
             del t2, b2
+        if w.d_qk in (128, 192):
+            also.append(time_rotate_quantize(w, max(20, args.steps // 5), warmup, device, peaks,
+                                             peak_src))
         extras["also"] = also
         extras["e2e"] = e2e_measure(w, t, max(5, min(50, args.steps // 10)), device)
         if world == 1:

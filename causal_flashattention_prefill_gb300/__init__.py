@@ -26,6 +26,7 @@ from ._lib import (  # noqa: F401
     zyfa_device_status,
     zyfa_fp8_quantize,
     zyfa_fp8_quantize_noalloc,
+    zyfa_fp8_quantize_rotated,
     zyfa_fp8_quantize_workspace_bytes,
     zyfa_fwd,
     zyfa_fwd_scaled,
@@ -42,4 +43,6 @@ from .api import (  # noqa: F401
     flash_attn_qkvpacked_func,
     flash_attn_varlen_func,
     fp8_quantize,
+    fp8_quantize_rotated,
+    hadamard_signs,
 )

@@ -44,6 +44,7 @@ SIGNATURES = {
     "zyfa_fp8_quantize": (_I, [_P, ctypes.c_longlong, _I, _P, _P, _P, _P]),
     "zyfa_fp8_quantize_workspace_bytes": (ctypes.c_longlong, []),
     "zyfa_fp8_quantize_noalloc": (_I, [_P, ctypes.c_longlong, _I, _P, _P, _P]),
+    "zyfa_fp8_quantize_rotated": (_I, [_P, ctypes.c_longlong, _I, _I, _P, _P, _P, _P, _P]),
 }
 
 _lib = None
@@ -115,3 +116,9 @@ def zyfa_fp8_quantize_workspace_bytes() -> int:
 
 def zyfa_fp8_quantize_noalloc(x, n, x_dtype, x8, descale, stream) -> int:
     return load().zyfa_fp8_quantize_noalloc(x, n, x_dtype, x8, descale, stream)
+
+
+def zyfa_fp8_quantize_rotated(x, n_rows, d, x_dtype, signs, x8, descale, workspace,
+                              stream) -> int:
+    return load().zyfa_fp8_quantize_rotated(x, n_rows, d, x_dtype, signs, x8, descale,
+                                            workspace, stream)

@@ -282,3 +282,51 @@ def flash_attn_varlen_func(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, ma
     if return_lse:
         return out, lse
     return out
+
+
+def hadamard_signs(d: int, seed: int = 0, device="cuda") -> torch.Tensor:
+    """The random signs s of R = diag(s) H / sqrt(d), drawn as the ZYFA README
+    draws them ("Using FP8 attention in a model": a seeded generator, one
+    matrix for every layer and head), as a float32 tensor on ``device``."""
+    g = torch.Generator().manual_seed(seed)
+    s = torch.randint(0, 2, (d,), generator=g) * 2 - 1
+    return s.to(dtype=torch.float32, device=device)
+
+
+def fp8_quantize_rotated(x: torch.Tensor, signs: torch.Tensor, workspace: torch.Tensor = None,
+                         stream=None):
+    """Rotation then per-tensor e4m3 quantisation, on the GPU, for q and k.
+
+    Each row of the last dimension d (128, or 192 in the DCT x Hadamard form)
+    becomes ``x @ R`` with ``R = diag(signs) H / sqrt(d)``; the result is
+    quantised like ``fp8_quantize``.  Rotate q and k with the same signs and
+    leave v unrotated: the scores are unchanged and the quantisation error
+    drops (ZYFA README, "Using FP8 attention in a model").  Returns
+    ``(x8, descale)``.
+    """
+    if x.dtype == torch.bfloat16:
+        xt = _lib.ZYFA_BF16
+    elif x.dtype == torch.float32:
+        xt = _lib.ZYFA_F32
+    else:
+        raise TypeError(f"fp8_quantize_rotated takes BF16 or float32, not {x.dtype}")
+    d = x.shape[-1]
+    if d not in (128, 192):
+        raise ValueError(f"the rotation is defined for d = 128 and d = 192, not {d}")
+    if signs.dtype != torch.float32 or signs.numel() != d or signs.device != x.device:
+        raise ValueError("signs must be d float32 values on x's device")
+    x = x.detach().contiguous()
+    signs = signs.contiguous()
+    x8 = torch.empty(x.shape, dtype=torch.float8_e4m3fn, device=x.device)
+    descale = torch.empty(1, dtype=torch.float32, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(_lib.zyfa_fp8_quantize_workspace_bytes(), dtype=torch.uint8,
+                                device=x.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device).cuda_stream
+    st = _lib.zyfa_fp8_quantize_rotated(x.data_ptr(), x.numel() // d, d, xt, signs.data_ptr(),
+                                        x8.data_ptr(), descale.data_ptr(), workspace.data_ptr(),
+                                        stream)
+    if st != _lib.ZYFA_OK:
+        raise ZyfaError(st)
+    return x8, descale

@@ -258,6 +258,24 @@ int zyfa_fp8_quantize_noalloc(const void* x, long long n, int x_dtype, void* x8,
   return e == 0 ? ZYFA_OK : ZYFA_ERR_LAUNCH;
 }
 
+int zyfa_fp8_quantize_rotated(const void* x, long long n_rows, int d, int x_dtype,
+                              const float* signs, void* x8, float* descale, void* workspace,
+                              struct CUstream_st* stream) {
+  if (!x || !signs || !x8 || !descale || !workspace || n_rows < 0) return ZYFA_ERR_ARG;
+  if (d != 128 && d != 192) return ZYFA_ERR_UNSUPPORTED;
+  if (x_dtype != ZYFA_BF16 && x_dtype != ZYFA_F32) return ZYFA_ERR_UNSUPPORTED;
+  if (n_rows > (1LL << 40) / d) return ZYFA_ERR_ARG;
+  if (!aligned(x, 16) || !aligned(x8, 8) || !aligned(descale, 4) || !aligned(workspace, 4) ||
+      !aligned(signs, 4))
+    return ZYFA_ERR_ALIGN;
+  const int sms = current_device_sms();
+  if (sms <= 0) return ZYFA_ERR_DEVICE;
+  const int e = zyfa::launch_fp8_quantize_rotated(
+      x, n_rows, d, x_dtype == ZYFA_BF16 ? zyfa::kQuantBF16 : zyfa::kQuantF32, signs, x8,
+      descale, static_cast<float*>(workspace), sms, reinterpret_cast<cudaStream_t>(stream));
+  return e == 0 ? ZYFA_OK : ZYFA_ERR_LAUNCH;
+}
+
 int zyfa_version(void) { return (1 << 16) | 1; }
 
 }  // extern "C"

@@ -15,6 +15,13 @@ constexpr int kQuantMaxPartials = 1024; // CTAs of the max pass = floats of work
 int launch_fp8_quantize(const void* x, int64_t n, int x_type, void* x8, float* descale,
                         float* partial, int sms, cudaStream_t stream);
 
+// Rows of d = 128 or 192 channels rotated by diag(signs) times the Hadamard
+// (d = 128) or DCT x Hadamard (d = 192) matrix, then quantised per tensor like
+// launch_fp8_quantize.  Returns a cudaError_t.
+int launch_fp8_quantize_rotated(const void* x, int64_t rows, int d, int x_type,
+                                const float* signs, void* x8, float* descale, float* partial,
+                                int sms, cudaStream_t stream);
+
 // Same, with the first pass's maxima in a file-scope device array instead of a
 // caller workspace (one-time symbol lookup per device on first use).  Sets
 // *too_large when the array cannot hold the first pass's maxima.

@@ -173,6 +173,39 @@ ZYFA_API long long zyfa_fp8_quantize_workspace_bytes(void);
 ZYFA_API int zyfa_fp8_quantize_noalloc(const void* x, long long n, int x_dtype, void* x8,
                                        float* descale, struct CUstream_st* stream);
 
+/*
+ * Rotation of q or k followed by per-tensor FP8 quantisation, in two kernels
+ * (ZYFA README, "Using FP8 attention in a model": a Hadamard rotation of q
+ * and k before quantisation roughly halves the input error, and fused into
+ * the pass that quantises q it costs little; v is left unrotated).  Each row
+ * of d channels is rotated as y = x @ R with
+ *
+ *   d = 128: R = diag(signs) H / sqrt(128), H Sylvester's Hadamard matrix
+ *            (H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]]);
+ *   d = 192: R = diag(signs) (C3^T kron H_64) / 8, C3 the orthonormal 3-point
+ *            DCT-II (C3[k][n] = a_k cos(pi (2n+1) k / 6), a_0 = sqrt(1/3),
+ *            a_k = sqrt(2/3)) -- the README combines a 3-point DCT with a
+ *            64-point Hadamard matrix for d = 192;
+ *
+ * then y is quantised exactly as zyfa_fp8_quantize does (power-of-two
+ * descale from max|y|, round to nearest even, saturating).  R is orthogonal,
+ * so rotating q and k with the same signs leaves q k^T unchanged.  The
+ * rotation is evaluated in FP32 (butterflies across the lanes of a warp).
+ *
+ * x          device, n_rows * d elements of x_dtype (ZYFA_BF16 or ZYFA_F32),
+ *            rows contiguous, 16-byte aligned.
+ * n_rows     number of rows (tokens x heads), >= 0.
+ * d          128 or 192 (others: ZYFA_ERR_UNSUPPORTED).
+ * signs      device, d FP32 values, each +1 or -1 (the same for q and k),
+ *            4-byte aligned.
+ * x8, descale, workspace, stream: as for zyfa_fp8_quantize (x8 holds
+ *            n_rows * d codes); deterministic (no atomics).
+ * Returns ZYFA_OK or a negative zyfa_status (checks run before any launch).
+ */
+ZYFA_API int zyfa_fp8_quantize_rotated(const void* x, long long n_rows, int d, int x_dtype,
+                                       const float* signs, void* x8, float* descale,
+                                       void* workspace, struct CUstream_st* stream);
+
 /* ABI version, (major << 16) | minor. */
 ZYFA_API int zyfa_version(void);
 

@@ -158,3 +158,28 @@ def test_quantize_rejects_before_any_cuda_call(lib, kw, expected):
 
 def test_quantize_workspace_size(lib):
     assert zf.zyfa_fp8_quantize_workspace_bytes() == 4096
+
+
+ROT_CASES = [
+    (dict(x=0), zf.ZYFA_ERR_ARG),
+    (dict(signs=0), zf.ZYFA_ERR_ARG),
+    (dict(x8=0), zf.ZYFA_ERR_ARG),
+    (dict(descale=0), zf.ZYFA_ERR_ARG),
+    (dict(ws=0), zf.ZYFA_ERR_ARG),
+    (dict(rows=-1), zf.ZYFA_ERR_ARG),
+    (dict(rows=1 << 40), zf.ZYFA_ERR_ARG),
+    (dict(d=64), zf.ZYFA_ERR_UNSUPPORTED),
+    (dict(d=256), zf.ZYFA_ERR_UNSUPPORTED),
+    (dict(dt=zf.ZYFA_FP8_E4M3), zf.ZYFA_ERR_UNSUPPORTED),
+    (dict(x=A + 8), zf.ZYFA_ERR_ALIGN),
+    (dict(x8=A + 4), zf.ZYFA_ERR_ALIGN),
+    (dict(signs=A + 2), zf.ZYFA_ERR_ALIGN),
+]
+
+
+@pytest.mark.parametrize("kw,expected", ROT_CASES, ids=[str(c[0]) for c in ROT_CASES])
+def test_rotated_quantize_rejects_before_any_cuda_call(lib, kw, expected):
+    a = dict(x=A, rows=64, d=128, dt=zf.ZYFA_BF16, signs=A, x8=A, descale=A, ws=A)
+    a.update(kw)
+    assert zf.zyfa_fp8_quantize_rotated(a["x"], a["rows"], a["d"], a["dt"], a["signs"], a["x8"],
+                                        a["descale"], a["ws"], 0) == expected
