@@ -219,11 +219,12 @@ template <class C, bool kExact, bool kTest = false>
 __device__ __forceinline__ void produce_half(const float* f, float c_log2, float neg_m,
                                              uint32_t t_s, int h, bool two_term,
                                              float2 (&sacc)[2], float& rr, uint32_t tk = 0,
-                                             uint32_t* tacc = nullptr) {
+                                             uint32_t* tacc = nullptr, int cc0 = 0,
+                                             int ncc = 2) {
   const float2 c2 = make_float2(c_log2, c_log2);
   const float2 nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
-  for (int cc = 0; cc < 2; ++cc) {
+  for (int cc = cc0; cc < cc0 + ncc; ++cc) {
     const int ch = 2 * h + cc;  // 32-column chunk of the row
     float e[32];
 #pragma unroll
@@ -651,18 +652,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ++s_uses;
         ptx::tc_fence_after();
-        // S row: columns 0..63 are loaded and waited for; 64..127 are
-        // requested at once and waited for after the first half's exp2.
+        // S row: columns 0..31 are loaded and waited for; 32..127 are
+        // requested at once and waited for after the first 32 exp2 (a
+        // tensor-memory load takes hundreds of cycles while the tensor core
+        // streams, so the wait covers as few columns as possible).
         uint32_t v[128];
-        ptx::tmem_ld64_wait(t_s, *reinterpret_cast<uint32_t(*)[64]>(&v[0]));
+        ptx::tmem_ld32_wait(t_s, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        ptx::tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
         ptx::tmem_ld64_nowait(t_s + 64, *reinterpret_cast<uint32_t(*)[64]>(&v[64]));
+        auto wait_rest = [&]() {
+          ptx::tmem_wait_ld_dep32(*reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          ptx::tmem_wait_ld_dep64(*reinterpret_cast<uint32_t(*)[64]>(&v[64]));
+        };
         float* f = reinterpret_cast<float*>(v);
         const bool diag = j == tile;
         if (diag) {
           // Diagonal tile: key column c is in the future of the row when
           // c exceeds the row's index in the tile.
+          wait_rest();
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
+          for (int c = 0; c < 128; ++c)
             if (c > row_in_tile) f[c] = -INFINITY;
         }
         // Accuracy of the rounded P (decided per warp from the tile's actual
@@ -680,12 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool exact = false, two_term = false;
         if (j == 0) {
           // First tile of the row: the reference is this tile's maximum.
-          ptx::tmem_wait_ld_dep64(*reinterpret_cast<uint32_t(*)[64]>(&v[64]));
-          if (diag) {
-#pragma unroll
-            for (int c = 64; c < 128; ++c)
-              if (c > row_in_tile) f[c] = -INFINITY;
-          }
+          wait_rest();
           m_ref = row_max128(f) * c_log2;
           exact = !C::kF8;
           two_term = C::kF8;
@@ -707,13 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t acc_code = ptx::pack_e4m3x4(l * (1.0f / C::kAccRatio), 0.f, 0.f, 0.f) & 0xFFu;
             tk = threshold_addend(acc_code < cap_code ? acc_code : cap_code);
           }
-          produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 0, false, sacc, rr, tk, &tacc);
-          ptx::tmem_wait_ld_dep64(*reinterpret_cast<uint32_t(*)[64]>(&v[64]));
-          if (diag) {
-#pragma unroll
-            for (int c = 64; c < 128; ++c)
-              if (c > row_in_tile) f[c] = -INFINITY;
-          }
+          produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 0, false, sacc, rr, tk, &tacc, 0, 1);
+          wait_rest();
+          produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 0, false, sacc, rr, tk, &tacc, 1, 1);
           produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 1, false, sacc, rr, tk, &tacc);
           const float2 t2 = __fadd2_rn(sacc[0], sacc[1]);
           rs = t2.x + t2.y;
