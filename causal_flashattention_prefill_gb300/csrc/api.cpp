@@ -134,6 +134,27 @@ int make_map(CUtensorMap* m, const void* base, int dtype, int layout, int B, int
   return r == CUDA_SUCCESS ? ZYFA_OK : ZYFA_ERR_ARG;
 }
 
+// 2-D map over rows of d channels (x_type elements, rows contiguous): box of
+// 64 rows x 128 bytes, 128-byte swizzle (the rotation kernels' tiles).  An
+// empty tensor still gets a valid map (one row); no copy is issued then.
+int make_rows_map(CUtensorMap* m, const void* base, int x_type, long long rows, int d) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return ZYFA_ERR_DEVICE;
+  const cuuint64_t e = x_type == zyfa::kQuantBF16 ? 2 : 4;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(d),
+                              static_cast<cuuint64_t>(rows > 0 ? rows : 1)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(d) * e};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(zyfa::rot_box_inner_elems(x_type)),
+                             static_cast<cuuint32_t>(zyfa::kRotBoxRows)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapDataType dt = x_type == zyfa::kQuantBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ZYFA_OK : ZYFA_ERR_ARG;
+}
+
 }  // namespace
 
 extern "C" {
@@ -213,7 +234,13 @@ const char* zyfa_status_string(int status) {
 
 int zyfa_device_status(int* value, int reset) {
   if (!value) return ZYFA_ERR_ARG;
-  return zyfa::read_device_status(value, reset) == 0 ? ZYFA_OK : ZYFA_ERR_DEVICE;
+  // The attention kernel and the rotation kernels keep separate words (one
+  // per translation unit); the reported word is their union.
+  int a = 0, r = 0;
+  if (zyfa::read_device_status(&a, reset) != 0) return ZYFA_ERR_DEVICE;
+  if (zyfa::read_rot_status(&r, reset) != 0) return ZYFA_ERR_DEVICE;
+  *value = a | r;
+  return ZYFA_OK;
 }
 
 int zyfa_set_option(int option, int value) {
@@ -265,14 +292,20 @@ int zyfa_fp8_quantize_rotated(const void* x, long long n_rows, int d, int x_dtyp
   if (d != 128 && d != 192) return ZYFA_ERR_UNSUPPORTED;
   if (x_dtype != ZYFA_BF16 && x_dtype != ZYFA_F32) return ZYFA_ERR_UNSUPPORTED;
   if (n_rows > (1LL << 40) / d) return ZYFA_ERR_ARG;
+  // Tile coordinates of the copies are 32-bit row indices.
+  if (n_rows > (1LL << 31) - 1 - zyfa::kRotBoxRows) return ZYFA_ERR_UNSUPPORTED;
   if (!aligned(x, 16) || !aligned(x8, 8) || !aligned(descale, 4) || !aligned(workspace, 4) ||
       !aligned(signs, 4))
     return ZYFA_ERR_ALIGN;
   const int sms = current_device_sms();
   if (sms <= 0) return ZYFA_ERR_DEVICE;
-  const int e = zyfa::launch_fp8_quantize_rotated(
-      x, n_rows, d, x_dtype == ZYFA_BF16 ? zyfa::kQuantBF16 : zyfa::kQuantF32, signs, x8,
-      descale, static_cast<float*>(workspace), sms, reinterpret_cast<cudaStream_t>(stream));
+  const int xt = x_dtype == ZYFA_BF16 ? zyfa::kQuantBF16 : zyfa::kQuantF32;
+  CUtensorMap tm;
+  const int me = make_rows_map(&tm, x, xt, n_rows, d);
+  if (me != ZYFA_OK) return me;
+  const int e = zyfa::launch_fp8_quantize_rotated(tm, n_rows, d, xt, signs, x8, descale,
+                                                  static_cast<float*>(workspace), sms,
+                                                  reinterpret_cast<cudaStream_t>(stream));
   return e == 0 ? ZYFA_OK : ZYFA_ERR_LAUNCH;
 }
 

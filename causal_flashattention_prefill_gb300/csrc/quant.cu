@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include "quant.h"
+#include "zyfa_ptx.cuh"
 
 namespace zyfa {
 namespace {
@@ -165,87 +166,81 @@ int launch_t(const void* x, int64_t n, void* x8, float* descale, float* partial,
 // model"): each row of d channels becomes x @ R, R = diag(s) H / sqrt(d) for
 // d = 128 (H: Sylvester's Hadamard matrix) and R = diag(s) (C3^T kron H_64) / 8
 // for d = 192 (C3: orthonormal 3-point DCT-II), then the rotated tensor is
-// quantised per tensor as above.  One thread per row: the row is loaded into
-// registers, multiplied by the signs (kept in shared memory), and transformed
-// by in-register butterflies (H_2n = [[H_n, H_n], [H_n, -H_n]]: at stride h,
-// channel pairs (i, i + h) with bit h of i clear become (a + b, a - b)); for
-// d = 192 each 64-channel block is transformed and the three blocks are mixed
-// by the DCT.  The first pass keeps max |x @ R|, the second recomputes the
-// rotation and stores the codes (16 per 16-byte store).
+// quantised per tensor as above.  The butterflies of H_2n = [[H_n, H_n],
+// [H_n, -H_n]] run in registers: at stride h, channel pairs (i, i + h) with
+// bit h of i clear become (a + b, a - b); for d = 192 each 64-channel block
+// is transformed and the three blocks are mixed by the DCT.  The first pass
+// keeps max |x @ R|, the second recomputes the rotation and stores the codes.
+//
+// Data movement: tiles of 64 rows stream through a ring of shared-memory
+// stages filled by TMA from a two-dimensional tensor map over (channels,
+// rows) with 128-byte swizzle, one box of 64 rows x 128 bytes per 128 bytes
+// of the row.  Warps 0-3 rotate 16 rows of each tile (lane = row lane & 15,
+// half lane >> 4); warp 4 issues the copies.  The eight lanes of a quarter
+// warp read 16-byte chunks of eight consecutive rows, which the swizzle
+// places in eight distinct bank groups, so the reads are conflict-free.
 
-constexpr int kRotThreads = 128;
-constexpr int kRotRowsPerCta = kRotThreads / 2;
+constexpr int kRotTileRows = 64;
+constexpr int kRotConsumers = 4;                       // warps that rotate
+constexpr int kRotThreads = 32 * (kRotConsumers + 1);  // + one producer warp
+constexpr int kRotSmemTarget = 64 * 1024;              // ring bytes per CTA (at least two stages)
 
-// Two lanes per row: lane half p = lane & 1 holds, for d = 128, channels
-// 64p .. 64p+63 (local index i -> channel 64p + i); for d = 192, channels
-// 64a + 32p .. 64a + 32p + 31 of each block a (local index 32a + i).  Every
-// butterfly stride but the largest of each Hadamard block stays inside the
-// lane; the largest (64 for d = 128, 32 for the 64-channel blocks of d = 192)
-// pairs the two lanes of the row (shuffle distance 1).
+// Status word of these kernels (bit 0: a wait timed out).
+__device__ int g_rot_status;
+
+template <int D, int XT>
+struct RotTile {
+  static constexpr int kElem = XT == kQuantBF16 ? 2 : 4;
+  static constexpr int kBoxElems = 128 / kElem;            // inner box extent
+  static constexpr int kBoxes = D * kElem / 128;           // boxes per row
+  static constexpr int kBoxBytes = kRotTileRows * 128;
+  static constexpr int kTileBytes = kBoxes * kBoxBytes;
+  static constexpr int kStagesFit = kRotSmemTarget / kTileBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : (kStagesFit < 2 ? 2 : kStagesFit);
+  static constexpr int kChunks = D * kElem / 2 / 16;       // 16-byte chunks of a half row
+  static constexpr int kPerChunk = 16 / kElem;             // values per chunk
+  static constexpr int kSmem = 1024 + kStages * kTileBytes + 2 * kStages * 8 + 16;
+  static_assert(D * kElem % 128 == 0, "whole boxes per row");
+  static_assert(kStages >= 2, "ring needs two stages");
+};
+
+// Lane half p of a row holds, for d = 128, channels 64p .. 64p+63 (local
+// index i -> channel 64p + i); for d = 192, channels 64a + 32p .. 64a + 32p +
+// 31 of each block a (local index 32a + i).  Every butterfly stride but the
+// largest of each Hadamard block stays inside the lane; the largest (64 for
+// d = 128, 32 for the 64-channel blocks of d = 192) pairs the two lanes of
+// the row (shuffle distance 16).
 template <int D>
 struct RotHalf {
-  static constexpr int kVals = D / 2;
   static constexpr int kBlock = D == 128 ? 64 : 32;  // contiguous channels per lane segment
   static __device__ __forceinline__ int channel(int i, int p) {
     return D == 128 ? 64 * p + i : 64 * (i / 32) + 32 * p + (i % 32);
   }
 };
 
-// Coalesced loads: a warp copies its 16 rows (contiguous in memory) into
-// shared memory with consecutive 16-byte chunks per lane, laid out by lane
-// (row r, half p -> lane 2r + p) with 16 bytes of padding per lane so that
-// the lanes' reads of their own halves hit distinct banks; then each lane
-// converts its half to FP32.
+// This lane's half of row r of a tile in shared memory (boxes of 64 rows x
+// 128 bytes, 128-byte swizzle: chunk c of a box row r sits at chunk c ^ (r & 7)),
+// converted to FP32.
 template <int D, int XT>
-struct RotStage {
-  static constexpr int kElem = XT == kQuantBF16 ? 2 : 4;
-  static constexpr int kRowBytes = D * kElem;
-  static constexpr int kHalfBytes = kRowBytes / 2;
-  static constexpr int kPitch = kHalfBytes + 16;
-  static constexpr int kWarpBytes = 32 * kPitch;
-  static_assert(kHalfBytes % 16 == 0 && (D == 128 || (kRowBytes / 6) % 16 == 0), "16-byte chunks");
-};
-
-template <int D, int XT>
-__device__ __forceinline__ void rot_stage_load(const void* x, int64_t row0, int64_t rows,
-                                               uint8_t* wsm, int lane, float (&v)[D / 2]) {
-  using T = RotStage<D, XT>;
-  constexpr int kChunksPerRow = T::kRowBytes / 16;
-  const uint8_t* src = static_cast<const uint8_t*>(x) + row0 * T::kRowBytes;
-  __syncwarp();  // the previous rows have been read out
-#pragma unroll 4
-  for (int c = lane; c < 16 * kChunksPerRow; c += 32) {
-    const int r = c / kChunksPerRow;
-    const int off = (c % kChunksPerRow) * 16;
-    if (row0 + r >= rows) continue;
-    int half, local;
-    if constexpr (D == 128) {
-      half = off / T::kHalfBytes;
-      local = off % T::kHalfBytes;
-    } else {
-      constexpr int kSeg = T::kRowBytes / 3;   // one 64-channel block
-      const int a = off / kSeg, pos = off % kSeg;
-      half = pos / (kSeg / 2);
-      local = a * (kSeg / 2) + pos % (kSeg / 2);
-    }
-    *reinterpret_cast<uint4*>(wsm + (2 * r + half) * T::kPitch + local) =
-        *reinterpret_cast<const uint4*>(src + static_cast<int64_t>(c) * 16);
-  }
-  __syncwarp();
-  const uint4* mine = reinterpret_cast<const uint4*>(wsm + lane * T::kPitch);
+__device__ __forceinline__ void rot_read_half(const uint8_t* tile, int r, int p,
+                                              float (&v)[D / 2]) {
+  using T = RotTile<D, XT>;
 #pragma unroll
-  for (int j = 0; j < T::kHalfBytes / 16; ++j) {
-    const uint4 w = mine[j];
+  for (int k = 0; k < T::kChunks; ++k) {
+    const int byte = RotHalf<D>::channel(k * T::kPerChunk, p) * T::kElem;
+    const int box = byte >> 7, c16 = (byte & 127) >> 4;
+    const uint4 w = *reinterpret_cast<const uint4*>(tile + box * T::kBoxBytes + r * 128 +
+                                                    ((c16 ^ (r & 7)) << 4));
     if constexpr (XT == kQuantBF16) {
       const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        v[8 * j + 2 * k] = __uint_as_float(u[k] << 16);
-        v[8 * j + 2 * k + 1] = __uint_as_float(u[k] & 0xFFFF0000u);
+      for (int q = 0; q < 4; ++q) {
+        v[8 * k + 2 * q] = __uint_as_float(u[q] << 16);
+        v[8 * k + 2 * q + 1] = __uint_as_float(u[q] & 0xFFFF0000u);
       }
     } else {
-      v[4 * j] = __uint_as_float(w.x); v[4 * j + 1] = __uint_as_float(w.y);
-      v[4 * j + 2] = __uint_as_float(w.z); v[4 * j + 3] = __uint_as_float(w.w);
+      v[4 * k] = __uint_as_float(w.x); v[4 * k + 1] = __uint_as_float(w.y);
+      v[4 * k + 2] = __uint_as_float(w.z); v[4 * k + 3] = __uint_as_float(w.w);
     }
   }
 }
@@ -277,27 +272,30 @@ __device__ __forceinline__ void fwht_local(float (&v)[M], int o) {
   }
 }
 
-// The butterfly stride that pairs the two lanes of a row: the lower half
-// keeps a + b, the upper a - b, i.e. v' = v * (+1 or -1) + partner, exactly
-// (one rounding), two channels per FP32x2 multiply-add.
+// The butterfly stride that pairs the two lanes of a row (lanes l and l ^ 16):
+// the lower half keeps a + b, the upper a - b, i.e. v' = v * (+1 or -1) +
+// partner, exactly (one rounding), two channels per FP32x2 multiply-add.
 template <int N>
 __device__ __forceinline__ void cross_half(float (&v)[N], int p) {
   const float sgn = p ? -1.0f : 1.0f;
   const float2 s2 = make_float2(sgn, sgn);
 #pragma unroll
   for (int i = 0; i < N; i += 2) {
-    const float o0 = __shfl_xor_sync(0xffffffffu, v[i], 1);
-    const float o1 = __shfl_xor_sync(0xffffffffu, v[i + 1], 1);
+    const float o0 = __shfl_xor_sync(0xffffffffu, v[i], 16);
+    const float o1 = __shfl_xor_sync(0xffffffffu, v[i + 1], 16);
     const float2 r = __ffma2_rn(make_float2(v[i], v[i + 1]), s2, make_float2(o0, o1));
     v[i] = r.x;
     v[i + 1] = r.y;
   }
 }
 
-// x @ R of the row, this lane's half, in place (s_signs: D signs in shared
-// memory, stored as [p][D/2 + 1] so that the two halves use different banks).
-// Adding +0 at the end makes an exactly zero result +0 (its sign would
-// otherwise depend on the order of the sums), so a zero always gets code 0x00.
+// x @ R of the row up to one constant factor per 32-channel block
+// (rot_scale), this lane's half, in place (s_signs: D signs in shared memory,
+// stored as [p][D/2 + 1] so that the two halves use different banks).  The
+// factor is applied by the passes: the max pass scales the maximum once
+// (rounding is monotonic, so the scaled maximum is the maximum of the scaled
+// values), the quantise pass folds it into the descale multiply (a power of
+// two, so one rounding gives the same value as two).
 template <int D>
 __device__ __forceinline__ void rot_half(float (&v)[D / 2], const float* s_signs, int p) {
   constexpr int kN = D / 2;
@@ -311,29 +309,29 @@ __device__ __forceinline__ void rot_half(float (&v)[D / 2], const float* s_signs
   if constexpr (D == 128) {
     fwht_local<64>(v, 0);
     cross_half<64>(v, p);
-    constexpr float kScale = 0.08838834764831845f;  // 1 / sqrt(128)
-    const float2 sc = make_float2(kScale, kScale), zero = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int i = 0; i < 64; i += 2) {
-      const float2 r = __ffma2_rn(make_float2(v[i], v[i + 1]), sc, zero);
-      v[i] = r.x;
-      v[i + 1] = r.y;
-    }
   } else {
 #pragma unroll
     for (int a = 0; a < 3; ++a) fwht_local<32>(v, 32 * a);
     cross_half<96>(v, p);
-    constexpr float kR3 = 0.57735026918962576f * 0.125f;   // 1/sqrt(3) / 8
-    constexpr float kR2 = 0.70710678118654752f * 0.125f;   // 1/sqrt(2) / 8
-    constexpr float kR6 = 0.40824829046386302f * 0.125f;   // 1/sqrt(6) / 8
+    // DCT rows (1, 1, 1), (1, 0, -1), (1, -2, 1) over the three blocks
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       const float b0 = v[e], b1 = v[32 + e], b2 = v[64 + e];
-      v[e] = (b0 + b1 + b2) * kR3 + 0.0f;
-      v[32 + e] = (b0 - b2) * kR2 + 0.0f;
-      v[64 + e] = (b0 - 2.0f * b1 + b2) * kR6 + 0.0f;
+      v[e] = (b0 + b1) + b2;
+      v[32 + e] = b0 - b2;
+      v[64 + e] = (b0 - 2.0f * b1) + b2;
     }
   }
+}
+
+// The factor of local 32-value block a: 1/sqrt(128) for d = 128; for d = 192
+// the DCT's row norms times 1/8 (H_64 / 8 is orthonormal).
+template <int D>
+__device__ __forceinline__ constexpr float rot_scale(int a) {
+  if (D == 128) return 0.08838834764831845f;            // 1 / sqrt(128)
+  return a == 0 ? 0.57735026918962576f * 0.125f          // 1/sqrt(3) / 8
+                : a == 1 ? 0.70710678118654752f * 0.125f  // 1/sqrt(2) / 8
+                         : 0.40824829046386302f * 0.125f; // 1/sqrt(6) / 8
 }
 
 template <int D>
@@ -353,127 +351,198 @@ __device__ __forceinline__ void rot_signs_to_smem(const float* signs, float* s_s
   }
 }
 
-template <int D, int XT>
-__global__ void __launch_bounds__(kRotThreads)
-    rot_amax_kernel(const void* x, int64_t rows, const float* signs, float* partial) {
-  __shared__ float s_signs[D + 2];
-  __shared__ float warp_max[kRotThreads / 32];
-  rot_signs_to_smem<D>(signs, s_signs);
-  __syncthreads();
-  const int p = threadIdx.x & 1;
-  const int lane = threadIdx.x & 31;
-  extern __shared__ __align__(16) uint8_t rot_smem[];
-  uint8_t* wsm = rot_smem + (threadIdx.x >> 5) * RotStage<D, XT>::kWarpBytes;
-  float m = 0.f;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kRotRowsPerCta;
-  // a warp takes 16 consecutive rows per iteration (row = row0 + lane / 2);
-  // the loop condition is warp-uniform
-  for (int64_t row0 = static_cast<int64_t>(blockIdx.x) * kRotRowsPerCta + (threadIdx.x >> 5) * 16;
-       row0 < rows; row0 += stride) {
-    float v[D / 2];
-    const bool live = row0 + (lane >> 1) < rows;
-    rot_stage_load<D, XT>(x, row0, rows, wsm, lane, v);
-    if (!live) {
-#pragma unroll
-      for (int i = 0; i < D / 2; ++i) v[i] = 0.f;
-    }
-    rot_half<D>(v, s_signs, p);
-#pragma unroll
-    for (int i = 0; i < D / 2; ++i) m = fmaxf(m, fabsf(v[i]));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float r = 0.f;
-    for (int i = 0; i < kRotThreads / 32; ++i) r = fmaxf(r, warp_max[i]);
-    partial[blockIdx.x] = r;
-  }
+// Waits with the whole warp (see the attention kernel's warp_wait): every
+// lane observes the completed phase, so the TMA-written tile is visible to
+// all of them.
+__device__ __forceinline__ bool rot_warp_wait(uint32_t b, uint32_t parity, volatile int* abort,
+                                              int lane) {
+  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(b, parity))) return true;
+  int ok = 0;
+  if (lane == 0) ok = ptx::mbar_wait(b, parity, abort, &g_rot_status, 1) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  if (ok) (void)ptx::mbar_test(b, parity);
+  return ok != 0;
 }
 
-template <int D, int XT>
+// One pass over the tensor.  kQuant = false: each CTA writes max |x @ R| of
+// its tiles to partial[blockIdx.x].  kQuant = true: every CTA reduces the
+// num_partials maxima to the descale, CTA 0 stores it, and each row's codes
+// are written to x8.  Tiles t = blockIdx.x + i * gridDim.x.
+template <int D, int XT, bool kQuant>
 __global__ void __launch_bounds__(kRotThreads)
-    rot_quant_kernel(const void* x, int64_t rows, const float* signs, uint8_t* x8,
-                     float* descale, const float* partial, int num_partials) {
+    rot_pass_kernel(const __grid_constant__ CUtensorMap tm, int64_t rows, const float* signs,
+                    float* partial, uint8_t* x8, float* descale, int num_partials) {
+  using T = RotTile<D, XT>;
+  constexpr int NS = T::kStages;
   __shared__ float s_signs[D + 2];
-  __shared__ float warp_max[kRotThreads / 32];
+  __shared__ float warp_max[kRotConsumers + 1];
   __shared__ float s_inv;
-  float m = 0.f;
-  for (int i = threadIdx.x; i < num_partials; i += kRotThreads) m = fmaxf(m, partial[i]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
-  rot_signs_to_smem<D>(signs, s_signs);
-  __syncthreads();
+  extern __shared__ uint8_t rot_raw[];
+  uint8_t* ring = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(rot_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + NS * T::kTileBytes);
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + 2 * NS);
+  const uint32_t bar0 = ptx::smem_u32(bars);
+  auto full = [&](int st) { return bar0 + 8u * static_cast<uint32_t>(st); };
+  auto empty = [&](int st) { return bar0 + 8u * static_cast<uint32_t>(NS + st); };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
   if (threadIdx.x == 0) {
-    float r = 0.f;
-    for (int i = 0; i < kRotThreads / 32; ++i) r = fmaxf(r, warp_max[i]);
-    const int k = descale_exponent(r);
-    s_inv = ldexpf(1.0f, -k);
-    if (blockIdx.x == 0) *descale = ldexpf(1.0f, k);
+    for (int st = 0; st < NS; ++st) {
+      ptx::mbar_init(full(st), 1);
+      ptx::mbar_init(empty(st), kRotConsumers);
+    }
+    *abort = 0;
+    ptx::fence_barrier_init();
+  }
+  rot_signs_to_smem<D>(signs, s_signs);
+  if constexpr (kQuant) {
+    float m = 0.f;
+    for (int i = threadIdx.x; i < num_partials; i += kRotThreads) m = fmaxf(m, partial[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) warp_max[warp] = m;
   }
   __syncthreads();
-  const float inv = s_inv;
-  const int p = threadIdx.x & 1;
-  constexpr int kSeg = RotHalf<D>::kBlock;
-  constexpr int kSegs = (D / 2) / kSeg;
-  const int lane = threadIdx.x & 31;
-  extern __shared__ __align__(16) uint8_t rot_smem[];
-  uint8_t* wsm = rot_smem + (threadIdx.x >> 5) * RotStage<D, XT>::kWarpBytes;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * kRotRowsPerCta;
-  for (int64_t row0 = static_cast<int64_t>(blockIdx.x) * kRotRowsPerCta + (threadIdx.x >> 5) * 16;
-       row0 < rows; row0 += stride) {
-    float v[D / 2];
-    const int64_t row = row0 + (lane >> 1);
-    const bool live = row < rows;
-    rot_stage_load<D, XT>(x, row0, rows, wsm, lane, v);
-    if (!live) {
-#pragma unroll
-      for (int i = 0; i < D / 2; ++i) v[i] = 0.f;
+  if constexpr (kQuant) {
+    if (threadIdx.x == 0) {
+      float r = 0.f;
+      for (int i = 0; i < kRotConsumers + 1; ++i) r = fmaxf(r, warp_max[i]);
+      const int k = descale_exponent(r);
+      s_inv = ldexpf(1.0f, -k);
+      if (blockIdx.x == 0) *descale = ldexpf(1.0f, k);
     }
-    rot_half<D>(v, s_signs, p);
-    if (live) {
+    __syncthreads();
+  }
+  const int64_t n_tiles = (rows + kRotTileRows - 1) / kRotTileRows;
+
+  if (warp == kRotConsumers) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tm);
+      // The first pass leaves x in L2 for the second where it fits; the
+      // second reads it for the last time.
+      const uint64_t pol = kQuant ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+      uint32_t armed = 0, par = 0;  // bit st: armed at least once / parity of its last arming
+      for (int64_t i = 0;; ++i) {
+        const int64_t tile = blockIdx.x + i * gridDim.x;
+        if (tile >= n_tiles) break;
+        const int st = static_cast<int>(i % NS);
+        const uint32_t round = static_cast<uint32_t>(i / NS);
+        if (!ptx::mbar_wait(empty(st), (round & 1u) ^ 1u, abort, &g_rot_status, 1)) break;
+        ptx::mbar_arrive_expect_tx(full(st), T::kTileBytes);
+        const uint32_t dst = ptx::smem_u32(ring + st * T::kTileBytes);
 #pragma unroll
-      for (int g = 0; g < kSegs; ++g) {
-        uint4* dst = reinterpret_cast<uint4*>(x8 + row * D + RotHalf<D>::channel(g * kSeg, p));
+        for (int bx = 0; bx < T::kBoxes; ++bx)
+          ptx::tma_load_2d(dst + bx * T::kBoxBytes, &tm, full(st), bx * T::kBoxElems,
+                           static_cast<int>(tile * kRotTileRows), pol);
+        armed |= 1u << st;
+        par = (par & ~(1u << st)) | ((round & 1u) << st);
+      }
+      // Every copy issued lands before the CTA's shared memory is released.
+      for (int st = 0; st < NS; ++st)
+        if ((armed >> st) & 1u) ptx::mbar_drain(full(st), (par >> st) & 1u);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ rotation
+    const int r = 16 * warp + (lane & 15);  // row within the tile
+    const int p = lane >> 4;                // half of the row
+    float m = 0.f;
+    for (int64_t i = 0;; ++i) {
+      const int64_t tile = blockIdx.x + i * gridDim.x;
+      if (tile >= n_tiles) break;
+      const int st = static_cast<int>(i % NS);
+      if (!rot_warp_wait(full(st), static_cast<uint32_t>(i / NS) & 1u, abort, lane)) break;
+      float v[D / 2];
+      rot_read_half<D, XT>(ring + st * T::kTileBytes, r, p, v);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(empty(st));
+      // Rows past the end read TMA's zero fill: they rotate to zero and
+      // leave the maximum unchanged; their codes are not stored.
+      rot_half<D>(v, s_signs, p);
+      if constexpr (!kQuant) {
 #pragma unroll
-        for (int j = 0; j < kSeg / 16; ++j) {
-          const float* w = v + g * kSeg + 16 * j;
-          uint4 o;
-          o.x = e4m3x4(w[0] * inv, w[1] * inv, w[2] * inv, w[3] * inv);
-          o.y = e4m3x4(w[4] * inv, w[5] * inv, w[6] * inv, w[7] * inv);
-          o.z = e4m3x4(w[8] * inv, w[9] * inv, w[10] * inv, w[11] * inv);
-          o.w = e4m3x4(w[12] * inv, w[13] * inv, w[14] * inv, w[15] * inv);
-          dst[j] = o;
+        for (int a = 0; a < D / 64; ++a) {
+          float mb = 0.f;
+#pragma unroll
+          for (int k = 0; k < 32; k += 2) mb = ptx::max3(mb, fabsf(v[32 * a + k]), fabsf(v[32 * a + k + 1]));
+          m = fmaxf(m, mb * rot_scale<D>(a));
+        }
+      } else {
+        const int64_t row = tile * kRotTileRows + r;
+        if (row < rows) {
+          const float inv = s_inv;
+          const float2 zero = make_float2(0.0f, 0.0f);
+          constexpr int kSeg = RotHalf<D>::kBlock;
+#pragma unroll
+          for (int g = 0; g < (D / 2) / kSeg; ++g) {
+            uint4* dst = reinterpret_cast<uint4*>(x8 + row * D + RotHalf<D>::channel(g * kSeg, p));
+#pragma unroll
+            for (int j = 0; j < kSeg / 16; ++j) {
+              // y = t * (factor * inv) + 0 (adding +0 makes an exactly zero
+              // result +0, whose sign would otherwise follow the order of the
+              // sums, so a zero always gets code 0x00)
+              const int i0 = g * kSeg + 16 * j;
+              const float c = rot_scale<D>(i0 / 32) * inv;
+              const float2 c2 = make_float2(c, c);
+              float y[16];
+#pragma unroll
+              for (int q = 0; q < 16; q += 2) {
+                const float2 r = __ffma2_rn(make_float2(v[i0 + q], v[i0 + q + 1]), c2, zero);
+                y[q] = r.x;
+                y[q + 1] = r.y;
+              }
+              uint4 o;
+              o.x = e4m3x4(y[0], y[1], y[2], y[3]);
+              o.y = e4m3x4(y[4], y[5], y[6], y[7]);
+              o.z = e4m3x4(y[8], y[9], y[10], y[11]);
+              o.w = e4m3x4(y[12], y[13], y[14], y[15]);
+              dst[j] = o;
+            }
+          }
         }
       }
     }
+    if constexpr (!kQuant) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) warp_max[warp] = m;
+    }
+  }
+  if constexpr (!kQuant) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float r = 0.f;
+      for (int i = 0; i < kRotConsumers; ++i) r = fmaxf(r, warp_max[i]);
+      partial[blockIdx.x] = r;
+    }
   }
 }
 
-int rot_grid(int64_t rows, int cap) {
-  const int64_t want = (rows + kRotRowsPerCta - 1) / kRotRowsPerCta;
-  if (want < 1) return 1;
-  return want < cap ? static_cast<int>(want) : cap;
-}
-
 template <int D, int XT>
-int launch_rot_t(const void* x, int64_t rows, const float* signs, void* x8, float* descale,
-                 float* partial, int sms, cudaStream_t s) {
-  const int g1 = rot_grid(rows, kQuantMaxPartials < 4 * sms ? kQuantMaxPartials : 4 * sms);
-  constexpr int kSmem = (kRotThreads / 32) * RotStage<D, XT>::kWarpBytes;
-  cudaError_t e = cudaFuncSetAttribute(rot_amax_kernel<D, XT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+int launch_rot_t(const CUtensorMap& tm, int64_t rows, const float* signs, void* x8,
+                 float* descale, float* partial, int sms, cudaStream_t s) {
+  using T = RotTile<D, XT>;
+  auto k1 = rot_pass_kernel<D, XT, false>;
+  auto k2 = rot_pass_kernel<D, XT, true>;
+  cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(rot_quant_kernel<D, XT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmem);
+  e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmem);
   if (e != cudaSuccess) return e;
-  rot_amax_kernel<D, XT><<<g1, kRotThreads, kSmem, s>>>(x, rows, signs, partial);
-  const int g2 = rot_grid(rows, 8 * sms);
-  rot_quant_kernel<D, XT><<<g2, kRotThreads, kSmem, s>>>(x, rows, signs,
-                                                         static_cast<uint8_t*>(x8), descale,
-                                                         partial, g1);
+  // Persistent grid: as many CTAs as are resident at once (both passes have
+  // the same footprint), so that the static deal of tiles has no second wave.
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k2, kRotThreads, T::kSmem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t n_tiles = (rows + kRotTileRows - 1) / kRotTileRows;
+  int cap = per_sm * sms;
+  if (cap > kQuantMaxPartials) cap = kQuantMaxPartials;
+  const int grid = n_tiles < 1 ? 1 : (n_tiles < cap ? static_cast<int>(n_tiles) : cap);
+  k1<<<grid, kRotThreads, T::kSmem, s>>>(tm, rows, signs, partial, nullptr, nullptr, 0);
+  k2<<<grid, kRotThreads, T::kSmem, s>>>(tm, rows, signs, partial, static_cast<uint8_t*>(x8),
+                                         descale, grid);
   return cudaGetLastError();
 }
 
@@ -486,18 +555,30 @@ int launch_fp8_quantize(const void* x, int64_t n, int x_type, void* x8, float* d
   return cudaErrorInvalidValue;
 }
 
-int launch_fp8_quantize_rotated(const void* x, int64_t rows, int d, int x_type,
+int launch_fp8_quantize_rotated(const CUtensorMap& tm, int64_t rows, int d, int x_type,
                                 const float* signs, void* x8, float* descale, float* partial,
                                 int sms, cudaStream_t stream) {
   if (d == 128 && x_type == kQuantBF16)
-    return launch_rot_t<128, kQuantBF16>(x, rows, signs, x8, descale, partial, sms, stream);
+    return launch_rot_t<128, kQuantBF16>(tm, rows, signs, x8, descale, partial, sms, stream);
   if (d == 128 && x_type == kQuantF32)
-    return launch_rot_t<128, kQuantF32>(x, rows, signs, x8, descale, partial, sms, stream);
+    return launch_rot_t<128, kQuantF32>(tm, rows, signs, x8, descale, partial, sms, stream);
   if (d == 192 && x_type == kQuantBF16)
-    return launch_rot_t<192, kQuantBF16>(x, rows, signs, x8, descale, partial, sms, stream);
+    return launch_rot_t<192, kQuantBF16>(tm, rows, signs, x8, descale, partial, sms, stream);
   if (d == 192 && x_type == kQuantF32)
-    return launch_rot_t<192, kQuantF32>(x, rows, signs, x8, descale, partial, sms, stream);
+    return launch_rot_t<192, kQuantF32>(tm, rows, signs, x8, descale, partial, sms, stream);
   return cudaErrorInvalidValue;
+}
+
+int rot_box_inner_elems(int x_type) { return x_type == kQuantBF16 ? 64 : 32; }
+
+int read_rot_status(int* value, int reset) {
+  cudaError_t e = cudaMemcpyFromSymbol(value, g_rot_status, sizeof(int));
+  if (e != cudaSuccess) return e;
+  if (reset) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_rot_status, &zero, sizeof(int));
+  }
+  return e;
 }
 
 }  // namespace zyfa

@@ -105,8 +105,9 @@ ZYFA_API const char* zyfa_status_string(int status);
 
 /*
  * Reads the device status word of the current device into *value (0 = no
- * wait has timed out; bit 0 = a kernel wait timed out) and clears it when
- * `reset` is non-zero.  Synchronous.  Returns ZYFA_OK or ZYFA_ERR_DEVICE.
+ * wait has timed out; bit 0 = a wait of the attention kernel or of the
+ * rotation kernels timed out) and clears it when `reset` is non-zero.
+ * Synchronous.  Returns ZYFA_OK or ZYFA_ERR_DEVICE.
  */
 ZYFA_API int zyfa_device_status(int* value, int reset);
 
@@ -191,10 +192,15 @@ ZYFA_API int zyfa_fp8_quantize_noalloc(const void* x, long long n, int x_dtype, 
  * descale from max|y|, round to nearest even, saturating).  R is orthogonal,
  * so rotating q and k with the same signs leaves q k^T unchanged.  The
  * rotation is evaluated in FP32 (butterflies across the lanes of a warp).
+ * Both kernels stream x in tiles of 64 rows through tensor-memory-access
+ * copies; their waits are bounded like the attention kernel's and report
+ * through zyfa_device_status().
  *
  * x          device, n_rows * d elements of x_dtype (ZYFA_BF16 or ZYFA_F32),
  *            rows contiguous, 16-byte aligned.
- * n_rows     number of rows (tokens x heads), >= 0.
+ * n_rows     number of rows (tokens x heads), >= 0; above 2^31 - 65
+ *            (row coordinates of the copies are 32-bit) the call returns
+ *            ZYFA_ERR_UNSUPPORTED.
  * d          128 or 192 (others: ZYFA_ERR_UNSUPPORTED).
  * signs      device, d FP32 values, each +1 or -1 (the same for q and k),
  *            4-byte aligned.

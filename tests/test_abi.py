@@ -168,6 +168,7 @@ ROT_CASES = [
     (dict(ws=0), zf.ZYFA_ERR_ARG),
     (dict(rows=-1), zf.ZYFA_ERR_ARG),
     (dict(rows=1 << 40), zf.ZYFA_ERR_ARG),
+    (dict(rows=1 << 31), zf.ZYFA_ERR_UNSUPPORTED),
     (dict(d=64), zf.ZYFA_ERR_UNSUPPORTED),
     (dict(d=256), zf.ZYFA_ERR_UNSUPPORTED),
     (dict(dt=zf.ZYFA_FP8_E4M3), zf.ZYFA_ERR_UNSUPPORTED),

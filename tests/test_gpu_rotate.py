@@ -77,6 +77,36 @@ def test_rotated_quantize_matches_oracle(d, dt, rows, scale):
     assert frac > 0.99
 
 
+@pytest.mark.parametrize("d,dt", [(128, torch.bfloat16), (192, torch.float32)], ids=["d128-bf16", "d192-f32"])
+def test_rotated_quantize_many_tiles_per_cta(d, dt):
+    # more 64-row tiles than CTAs x ring stages, so every CTA's ring wraps
+    # several times, with a ragged last tile
+    rows = 140001 if d == 128 else 60017
+    x = (workloads.gaussian((rows, d), 77 + d) * 2.0).to(dt)
+    signs = zf.hadamard_signs(d, seed=11)
+    x8, ds = zf.fp8_quantize_rotated(x.cuda(), signs)
+    torch.cuda.synchronize()
+    frac = _check_against_oracle(x.double().numpy(), signs.cpu().double().numpy(),
+                                 x8.view(torch.uint8).cpu().numpy(), float(ds.item()))
+    assert frac > 0.99
+
+
+def test_rotated_quantize_zero_rows():
+    # n_rows = 0 through the C ABI: descale 1, no code written, no wait timed out
+    x = torch.ones(64, 128, dtype=torch.bfloat16, device="cuda")
+    x8 = torch.full((64, 128), 0x55, dtype=torch.uint8, device="cuda")
+    ds = torch.zeros(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(zf.zyfa_fp8_quantize_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    signs = zf.hadamard_signs(128)
+    st = zf.zyfa_fp8_quantize_rotated(x.data_ptr(), 0, 128, zf.ZYFA_BF16, signs.data_ptr(),
+                                      x8.data_ptr(), ds.data_ptr(), ws.data_ptr(),
+                                      torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == zf.ZYFA_OK and float(ds.item()) == 1.0
+    assert int(x8.min()) == 0x55 and int(x8.max()) == 0x55
+    assert zf.zyfa_device_status(reset=True) == (zf.ZYFA_OK, 0)
+
+
 def test_rotated_quantize_activation_like_and_zero():
     # outlier channels (the case rotation is for) and an all-zero tensor
     g = torch.Generator().manual_seed(5)
