@@ -84,15 +84,16 @@ struct Cfg {
   // Lazy-rescale threshold in base-2 units of the score (the ZYFA README's
   // "Kernel design" uses 0.125-8).  Large thresholds keep the reference
   // from moving after the first tiles, so exp2 can run against it before
-  // the tile maximum is known: BF16 8 (p <= 256), FP8 4 (p * 2^4 <= 256,
-  // inside e4m3's 448).
-  static constexpr float kTau = kF8 ? 4.0f : 8.0f;
+  // the tile maximum is known: BF16 16 (p <= 2^16, far inside BF16 and the
+  // FP32 sums and accumulators), FP8 4 (p * 2^4 <= 256, inside e4m3's 448).
+  static constexpr int kTauBits = kF8 ? 4 : 16;
+  static constexpr float kTau = static_cast<float>(kTauBits);
   // FP8 P is stored as e4m3 of p * 2^4 (p <= 2^tau keeps it below 448); the
   // factor enters as +4 in the exponent.
-  static constexpr float kPLog2Scale = kF8 ? 4.0f : 0.0f;
+  static constexpr int kPLog2Bits = kF8 ? 4 : 0;
+  static constexpr float kPLog2Scale = static_cast<float>(kPLog2Bits);
   // Largest p that needs no rescale: 2^(tau + pre-scale).
-  static constexpr float kPCap = 256.0f;
-  static_assert(kTau + kPLog2Scale == 8.0f, "kPCap is 2^(tau + pre-scale)");
+  static constexpr float kPCap = static_cast<float>(1u << (kTauBits + kPLog2Bits));
   // Accuracy test: a p above 1/kAccRatio of the row's mass so far takes the
   // exact path (BF16 rounded-sum denominator, FP8 two-term P).
   static constexpr float kAccRatio = kF8 ? 32.0f : 8.0f;
@@ -319,20 +320,15 @@ __device__ __forceinline__ float rounded_sum_bf16(const float* f, float c_log2, 
 }
 
 // P for the whole 128-score row against reference neg_m; rs = unrounded
-// sum, rr = sum of the rounded values (when `heavy`, BF16).
-template <class C>
+// sum, rr = sum of the rounded values (with kRR, BF16).  The variant is a
+// template argument so that each call site carries only the code it runs.
+template <class C, bool kRR>
 __device__ __forceinline__ void produce_tile(const float* f, float c_log2, float neg_m,
-                                             uint32_t t_s, bool heavy, bool two_term, float& rs,
-                                             float& rr) {
+                                             uint32_t t_s, bool two_term, float& rs, float& rr) {
   float2 sacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   rr = 0.f;
-  if (heavy) {
-    produce_half<C, true>(f, c_log2, neg_m, t_s, 0, two_term, sacc, rr);
-    produce_half<C, true>(f, c_log2, neg_m, t_s, 1, two_term, sacc, rr);
-  } else {
-    produce_half<C, false>(f, c_log2, neg_m, t_s, 0, two_term, sacc, rr);
-    produce_half<C, false>(f, c_log2, neg_m, t_s, 1, two_term, sacc, rr);
-  }
+  produce_half<C, kRR>(f, c_log2, neg_m, t_s, 0, two_term, sacc, rr);
+  produce_half<C, kRR>(f, c_log2, neg_m, t_s, 1, two_term, sacc, rr);
   const float2 t2 = __fadd2_rn(sacc[0], sacc[1]);
   rs = t2.x + t2.y;
 }
@@ -693,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = row_max128(f) * c_log2;
           exact = !C::kF8;
           two_term = C::kF8;
-          produce_tile<C>(f, c_log2, C::kPLog2Scale - m_ref, t_s, exact, two_term, rs, rr);
+          produce_tile<C, !C::kF8>(f, c_log2, C::kPLog2Scale - m_ref, t_s, two_term, rs, rr);
         } else {
           // Exp2 against the current reference while the tile maximum is
           // formed; a tile whose maximum passes the reference by more than
@@ -725,7 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float bound = rs * 1.001f;
           const bool quiet = C::kF8 ? (tacc & 0x80808080u) == 0u
                                     : (bound <= C::kPCap && bound * C::kAccRatio <= l + rs);
-          if ((C::kF8 && diag) || !__all_sync(0xffffffffu, quiet)) {
+          if (diag || !__all_sync(0xffffffffu, quiet)) {
           const float mx = row_max128(f) * c_log2;
           const bool need = mx > m_ref + C::kTau;
           if (__any_sync(0xffffffffu, need)) {
@@ -749,7 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the speculative stores to the same columns have completed.
             ptx::tmem_wait_st();
             neg_m = C::kPLog2Scale - m_ref;
-            produce_tile<C>(f, c_log2, neg_m, t_s, false, false, rs, rr);
+            produce_tile<C, false>(f, c_log2, neg_m, t_s, false, rs, rr);
           }
           const float p_max = ptx::ex2(mx + neg_m);   // largest p of the tile (x pre-scale)
           if constexpr (C::kF8) {
