@@ -279,29 +279,43 @@ __device__ __forceinline__ uint32_t threshold_addend(uint32_t c) {
   return (0x80u - c) * 0x01010101u;
 }
 
-// FP8: the e4m3 rounding residual of P (lo term) for the 128 scores of the
-// row, recomputed from the scores exactly as the hi term was, stored at
-// column offset 32 of S.
+// FP8: the lo term of the row's P (the e4m3 rounding residual of hi, stored
+// at column offset 32 of S), and with do_hi also the hi term and its
+// unrounded sum rs, from one exp2 pass (hi and rs are the values, in the
+// same order, that produce_tile gives).  Without do_hi the hi codes in
+// tensor memory are those this pass would store.
 template <class C>
-__device__ __forceinline__ void store_lo_fp8(const float* f, float c_log2, float neg_m,
-                                             uint32_t t_s) {
+__device__ __forceinline__ void redo_fp8(const float* f, float c_log2, float neg_m,
+                                         uint32_t t_s, bool do_hi, float& rs) {
   const float2 c2 = make_float2(c_log2, c_log2);
   const float2 nm2 = make_float2(neg_m, neg_m);
+  float2 sacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
   for (int ch = 0; ch < 4; ++ch) {
-    uint32_t lo[8];
+    uint32_t hi[8], lo[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float2 xa = __ffma2_rn(make_float2(f[32 * ch + 4 * i], f[32 * ch + 4 * i + 1]), c2, nm2);
+      const float2 xa =
+          __ffma2_rn(make_float2(f[32 * ch + 4 * i], f[32 * ch + 4 * i + 1]), c2, nm2);
       const float2 xb =
           __ffma2_rn(make_float2(f[32 * ch + 4 * i + 2], f[32 * ch + 4 * i + 3]), c2, nm2);
       const float e0 = ptx::ex2(xa.x), e1 = ptx::ex2(xa.y), e2 = ptx::ex2(xb.x),
                   e3 = ptx::ex2(xb.y);
+      if (do_hi) {
+        sacc[0] = __fadd2_rn(sacc[0], make_float2(e0, e1));
+        sacc[1] = __fadd2_rn(sacc[1], make_float2(e2, e3));
+      }
+      hi[i] = ptx::pack_e4m3x4(e0, e1, e2, e3);
       float d[4];
-      ptx::unpack_e4m3x4(ptx::pack_e4m3x4(e0, e1, e2, e3), d);
+      ptx::unpack_e4m3x4(hi[i], d);
       lo[i] = ptx::pack_e4m3x4(e0 - d[0], e1 - d[1], e2 - d[2], e3 - d[3]);
     }
+    if (do_hi) ptx::tmem_st8(t_s + ch * 8, hi);
     ptx::tmem_st8(t_s + 32 + ch * 8, lo);
+  }
+  if (do_hi) {
+    const float2 t2 = __fadd2_rn(sacc[0], sacc[1]);
+    rs = t2.x + t2.y;
   }
 }
 
@@ -724,7 +738,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (diag || !__all_sync(0xffffffffu, quiet)) {
           const float mx = row_max128(f) * c_log2;
           const bool need = mx > m_ref + C::kTau;
-          if (__any_sync(0xffffffffu, need)) {
+          const bool any_need = __any_sync(0xffffffffu, need);
+          if (any_need) {
             const float alpha = need ? ptx::ex2(m_ref - mx) : 1.0f;
             if (need) {
               l *= alpha;
@@ -745,12 +760,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the speculative stores to the same columns have completed.
             ptx::tmem_wait_st();
             neg_m = C::kPLog2Scale - m_ref;
-            produce_tile<C, false>(f, c_log2, neg_m, t_s, false, rs, rr);
+            if constexpr (!C::kF8) produce_tile<C, false>(f, c_log2, neg_m, t_s, false, rs, rr);
           }
           const float p_max = ptx::ex2(mx + neg_m);   // largest p of the tile (x pre-scale)
           if constexpr (C::kF8) {
-            two_term = diag || __any_sync(0xffffffffu, p_max * 32.0f > l + rs);
-            if (two_term) store_lo_fp8<C>(f, c_log2, neg_m, t_s);
+            // A recomputed tile takes the two-term P in the same exp2 pass
+            // (right after a rescale its maximum carries most of the mass
+            // the row has seen, so the test below would pass anyway).
+            two_term = any_need || diag || __any_sync(0xffffffffu, p_max * 32.0f > l + rs);
+            if (two_term) redo_fp8<C>(f, c_log2, neg_m, t_s, any_need, rs);
           } else {
             exact = __any_sync(0xffffffffu, p_max * 8.0f > l + rs);
             if (exact) rr = rounded_sum_bf16(f, c_log2, neg_m);
