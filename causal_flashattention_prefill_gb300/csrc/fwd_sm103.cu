@@ -319,18 +319,36 @@ __device__ __forceinline__ void redo_fp8(const float* f, float c_log2, float neg
   }
 }
 
-// BF16: the sum of the rounded P of the row (the values that multiply V),
-// recomputed from the scores exactly as P was.
-__device__ __forceinline__ float rounded_sum_bf16(const float* f, float c_log2, float neg_m) {
+// BF16: the sum rr of the rounded P of the row (the values that multiply
+// V), and with do_hi also P itself (stored over S) and its unrounded sum rs,
+// from one exp2 pass (P and rs are the values, in the same order, that
+// produce_tile gives).  Without do_hi the P in tensor memory is the one this
+// pass would store.
+__device__ __forceinline__ void redo_bf16(const float* f, float c_log2, float neg_m,
+                                          uint32_t t_s, bool do_hi, float& rs, float& rr) {
   const float2 c2 = make_float2(c_log2, c_log2);
   const float2 nm2 = make_float2(neg_m, neg_m);
+  float2 sacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
   float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int i = 0; i < 64; ++i) {
-    const float2 x = __ffma2_rn(make_float2(f[2 * i], f[2 * i + 1]), c2, nm2);
-    a[i & 3] = ptx::add_bf16x2_f32(a[i & 3], ptx::pack_bf16x2(ptx::ex2(x.x), ptx::ex2(x.y)));
+  for (int ch = 0; ch < 4; ++ch) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int q = 16 * ch + i;  // pair index in the row
+      const float2 x = __ffma2_rn(make_float2(f[2 * q], f[2 * q + 1]), c2, nm2);
+      const float e0 = ptx::ex2(x.x), e1 = ptx::ex2(x.y);
+      if (do_hi) sacc[i & 1] = __fadd2_rn(sacc[i & 1], make_float2(e0, e1));
+      pk[i] = ptx::pack_bf16x2(e0, e1);
+      a[q & 3] = ptx::add_bf16x2_f32(a[q & 3], pk[i]);
+    }
+    if (do_hi) ptx::tmem_st16(t_s + ch * 16, pk);
   }
-  return (a[0] + a[1]) + (a[2] + a[3]);
+  rr = (a[0] + a[1]) + (a[2] + a[3]);
+  if (do_hi) {
+    const float2 t2 = __fadd2_rn(sacc[0], sacc[1]);
+    rs = t2.x + t2.y;
+  }
 }
 
 // P for the whole 128-score row against reference neg_m; rs = unrounded
@@ -755,12 +773,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
               ptx::tmem_st32(t_o + c * 32, o);
             }
-            // P of this tile again, against the moved reference (exactly
-            // the values a non-speculative pass would have produced), after
-            // the speculative stores to the same columns have completed.
+            // P of this tile is computed again below (redo_*) against the
+            // moved reference, exactly the values a non-speculative pass
+            // would have produced, once the speculative stores to the same
+            // columns have completed.
             ptx::tmem_wait_st();
             neg_m = C::kPLog2Scale - m_ref;
-            if constexpr (!C::kF8) produce_tile<C, false>(f, c_log2, neg_m, t_s, false, rs, rr);
           }
           const float p_max = ptx::ex2(mx + neg_m);   // largest p of the tile (x pre-scale)
           if constexpr (C::kF8) {
@@ -770,8 +788,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             two_term = any_need || diag || __any_sync(0xffffffffu, p_max * 32.0f > l + rs);
             if (two_term) redo_fp8<C>(f, c_log2, neg_m, t_s, any_need, rs);
           } else {
-            exact = __any_sync(0xffffffffu, p_max * 8.0f > l + rs);
-            if (exact) rr = rounded_sum_bf16(f, c_log2, neg_m);
+            // A recomputed tile takes the rounded-sum denominator in the same
+            // exp2 pass (right after a rescale its maximum carries most of
+            // the mass the row has seen, so the test would pass anyway).
+            exact = any_need || __any_sync(0xffffffffu, p_max * 8.0f > l + rs);
+            if (exact) redo_bf16(f, c_log2, neg_m, t_s, any_need, rs, rr);
           }
           }
         }
