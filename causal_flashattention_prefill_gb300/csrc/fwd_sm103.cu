@@ -57,6 +57,13 @@ constexpr int kBN = 128;  // keys per K/V tile
 constexpr int kDV = 128;
 constexpr int kMaxDynSmem = 232448;
 
+// 2^n as a float, for compile-time constants.
+constexpr float exp2i(int n) {
+  float r = 1.0f;
+  for (int i = 0; i < n; ++i) r *= 2.0f;
+  return r;
+}
+
 template <int DT, int DQK>
 struct Cfg {
   static constexpr bool kF8 = DT == 1;
@@ -93,7 +100,7 @@ struct Cfg {
   static constexpr int kPLog2Bits = kF8 ? 4 : 0;
   static constexpr float kPLog2Scale = static_cast<float>(kPLog2Bits);
   // Largest p that needs no rescale: 2^(tau + pre-scale).
-  static constexpr float kPCap = static_cast<float>(1u << (kTauBits + kPLog2Bits));
+  static constexpr float kPCap = exp2i(kTauBits + kPLog2Bits);
   // Accuracy test: a p above 1/kAccRatio of the row's mass so far takes the
   // exact path (BF16 rounded-sum denominator, FP8 two-term P).
   static constexpr float kAccRatio = kF8 ? 32.0f : 8.0f;
