@@ -87,7 +87,22 @@ struct Cfg {
   static constexpr int kReserve = 2048;       // alignment slack + barriers
   static constexpr int kSlotsFit = (kMaxDynSmem - kReserve - 2 * kTileBytesQK) / kSlotBytes;
   static constexpr int kNumSlots = kSlotsFit > 8 ? 8 : kSlotsFit;
-  static constexpr int kSmemBytes = kReserve + 2 * kTileBytesQK + kNumSlots * kSlotBytes;
+  // The K/V ring is a FIFO of pieces; a K tile takes kPiecesK consecutive
+  // pieces and a V tile kPiecesV.  Where whole-tile slots would leave no
+  // room to load ahead (fewer than three fit: BF16 d_qk = 192, whose Q tiles
+  // take 96 KB), a piece is one 16 KB chunk of a tile (128 rows x 128 bytes),
+  // so the next tiles start loading while the current ones are in use;
+  // elsewhere a piece is a whole-tile slot.
+  static constexpr bool kChunkPieces = kSlotsFit < 3;
+  static constexpr int kPieceBytes = kChunkPieces ? 128 * 128 : kSlotBytes;
+  static constexpr int kCppK = kChunkPieces ? 1 : kChunksQK;  // K chunks per piece
+  static constexpr int kCppV = kChunkPieces ? 1 : kChunksV;   // V chunks per piece
+  static constexpr int kPiecesK = kChunksQK / kCppK;
+  static constexpr int kPiecesV = kChunksV / kCppV;
+  static constexpr int kPiecesFit = (kMaxDynSmem - kReserve - 2 * kTileBytesQK) / kPieceBytes;
+  static constexpr int kNumPieces =
+      kChunkPieces ? (kPiecesFit > 8 ? 8 : kPiecesFit) : kNumSlots;
+  static constexpr int kSmemBytes = kReserve + 2 * kTileBytesQK + kNumPieces * kPieceBytes;
   // Lazy-rescale threshold in base-2 units of the score (the ZYFA README's
   // "Kernel design" uses 0.125-8).  Large thresholds keep the reference
   // from moving after the first tiles, so exp2 can run against it before
@@ -114,8 +129,13 @@ struct Cfg {
   static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
   static_assert(kNumSlots >= 2, "K/V ring needs at least two slots");
+  static_assert(!kChunkPieces || (kChunkBytesQK == kPieceBytes && kChunkBytesV == kPieceBytes),
+                "chunk pieces hold one chunk each");
+  static_assert(kNumPieces >= kPiecesK + 2 * kPiecesV,
+                "ring holds a V tile, the next K tile and a V tile with a skipped piece");
+  static_assert(kNumPieces <= 8, "ring bookkeeping packs 4 bits per piece");
   static_assert(kSmemBytes <= kMaxDynSmem, "shared memory budget");
-  static_assert(kSlotBytes % 1024 == 0 && kTileBytesQK % 1024 == 0, "1 KB alignment");
+  static_assert(kPieceBytes % 1024 == 0 && kTileBytesQK % 1024 == 0, "1 KB alignment");
 };
 
 struct Item {
@@ -170,6 +190,46 @@ struct Bars {
   static constexpr int kSlotFull = 13;        // [NS]
   static constexpr int kSlotEmpty = 13 + NS;  // [NS]
   static constexpr int kCount = 13 + 2 * NS;
+};
+
+// Placement of K/V tiles in the ring.  The producer and the MMA issuer walk
+// the same tile sequence (K_0, then V_j and K_j+1 for each step j, item
+// after item) and place each tile with this, so they agree on every piece.
+// Pieces are taken in cyclic order and released in the same order.
+template <class C>
+struct Ring {
+  uint32_t pc = 0;  // next free piece
+  // Places a K tile (v = false) or a V tile (v = true).  Returns its first
+  // occupied piece, whose full and empty barriers the tile uses; `base` is
+  // the piece of its chunk 0 and `last` its last occupied piece.  The chunks
+  // of a V tile are one MMA operand with a fixed stride, so a V tile that
+  // would wrap around the ring skips to piece 0 and keeps the skipped
+  // pieces; K chunks are separate operands and may wrap.
+  __device__ __forceinline__ uint32_t place(bool v, uint32_t& base, uint32_t& last) {
+    constexpr uint32_t np = C::kNumPieces;
+    const uint32_t n = v ? C::kPiecesV : C::kPiecesK;
+    const uint32_t first = pc;
+    base = (v && pc + n > np) ? 0u : pc;
+    pc = base + n;
+    if (pc >= np) pc -= np;            // base + n < 2 np: no division
+    last = pc == 0 ? np - 1 : pc - 1;
+    return first;
+  }
+  // Shared-memory byte offset (from the ring start) of chunk c of a tile
+  // whose chunk 0 is in piece `base` (c a compile-time constant at every
+  // call site, so the slot form is one multiply-add).
+  static __device__ __forceinline__ uint32_t k_chunk(uint32_t base, int c) {
+    if constexpr (!C::kChunkPieces) {
+      return base * C::kPieceBytes + c * C::kChunkBytesQK;
+    } else {
+      uint32_t q = base + c;
+      if (q >= C::kNumPieces) q -= C::kNumPieces;
+      return q * C::kPieceBytes;
+    }
+  }
+  static __device__ __forceinline__ uint32_t v_chunk(uint32_t base, int c) {
+    return (base + c / C::kCppV) * C::kPieceBytes + (c % C::kCppV) * C::kChunkBytesV;
+  }
 };
 
 __device__ __forceinline__ void tma_tile(const CUtensorMap* m, uint32_t dst, uint32_t bar,
@@ -380,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = Cfg<DT, DQK>;
-  constexpr int NS = C::kNumSlots;
+  constexpr int NS = C::kNumPieces;
   using B = Bars<NS>;
 
   extern __shared__ uint8_t smem_raw[];
@@ -390,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.q[0] = base;
   sm.q[1] = base + C::kTileBytesQK;
   sm.slots = base + 2 * C::kTileBytesQK;
-  sm.bars = reinterpret_cast<uint64_t*>(sm.slots + NS * C::kSlotBytes);
+  sm.bars = reinterpret_cast<uint64_t*>(sm.slots + NS * C::kPieceBytes);
   sm.tmem_base = reinterpret_cast<uint32_t*>(sm.bars + B::kCount);
   sm.abort = reinterpret_cast<int*>(sm.tmem_base + 1);
   sm.pflag = reinterpret_cast<volatile uint32_t*>(sm.abort + 1);
@@ -457,14 +517,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_kv = ptx::policy_evict_last();
       uint32_t q_par = 0;   // bit s: parity of the uses of Q buffer s so far
       uint32_t q_used = 0;  // bit s: Q buffer s was loaded at least once
-      uint32_t t = 0;       // K/V tiles issued so far (ring position)
+      uint32_t t = 0;       // slot ring: K/V tiles issued so far (ring position)
+      Ring<C> ring;         // chunk-piece ring: placement
       // The MMA issuer consumes the tiles in units: K_0 alone, then
       // (V_j, K_j+1) in step j.  Each unit completes on the full barrier of
-      // its first slot (armed with the bytes of the whole unit), so the
-      // issuer waits once per step.  fpar bit x: phase parity of slot x's
-      // full barrier after its last arming; armed bit x: armed at least once.
+      // its first tile (armed with the bytes of the whole unit), so the
+      // issuer waits once per step.  fpar bit x: phase parity of full
+      // barrier x after its last arming; armed bit x: armed at least once.
       uint32_t fpar = 0, armed = 0;
       uint32_t unit_bar = 0;
+      // Piece ownership: the tile that last took piece q releases it on the
+      // empty barrier own_b[q] (4 bits per piece) with phase parity
+      // own_par bit q; own_valid bit q: piece q was ever taken.  rel_par bit
+      // x: parity of the next release phase of empty barrier x.  Pieces are
+      // taken and released in the same cyclic order, so a tile needs only
+      // the release of the newest earlier owner among its pieces: the owner
+      // of its last piece.
+      uint32_t own_b = 0, own_par = 0, own_valid = 0, rel_par = 0;
       const int group = p.H / p.Hkv;
       bool ok = true;
       for (int r = 0; ok; ++r) {
@@ -487,45 +556,91 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_used |= 1u << s;
         }
         const int hk = it.h / group;
-        for (int j = 0; j < it.nload && ok; ++j) {
-          for (int kv = 0; kv < 2; ++kv) {
-            const uint32_t slot = t % NS;
-            ok = ptx::mbar_wait(bar(B::kSlotEmpty + slot), ((t / NS) & 1u) ^ 1u, abort, status,
-                                1);
-            if (!ok) break;
-            const uint32_t dst = slots_smem + slot * C::kSlotBytes;
-            if (kv == 0) {
-              uint32_t fb = unit_bar;  // K_j, j > 0: second tile of the unit (V_j-1, K_j)
-              if (j == 0) {
-                fb = bar(B::kSlotFull + slot);
-                ptx::mbar_arrive_expect_tx(fb, C::kTileBytesQK);
+        if constexpr (!C::kChunkPieces) {
+          for (int j = 0; j < it.nload && ok; ++j) {
+            for (int kv = 0; kv < 2; ++kv) {
+              const uint32_t slot = t % NS;
+              ok = ptx::mbar_wait(bar(B::kSlotEmpty + slot), ((t / NS) & 1u) ^ 1u, abort, status,
+                                  1);
+              if (!ok) break;
+              const uint32_t dst = slots_smem + slot * C::kSlotBytes;
+              if (kv == 0) {
+                uint32_t fb = unit_bar;  // K_j, j > 0: second tile of the unit (V_j-1, K_j)
+                if (j == 0) {
+                  fb = bar(B::kSlotFull + slot);
+                  ptx::mbar_arrive_expect_tx(fb, C::kTileBytesQK);
+                  fpar ^= 1u << slot;
+                  armed |= 1u << slot;
+                }
+  #pragma unroll
+                for (int c = 0; c < C::kChunksQK; ++c)
+                  tma_tile(&tm_k, dst + c * C::kChunkBytesQK, fb, p.layout,
+                           c * C::kChunkElemsQK, hk, j * kBN, it.b, pol_kv);
+              } else {
+                const uint32_t fb = bar(B::kSlotFull + slot);
+                ptx::mbar_arrive_expect_tx(
+                    fb, C::kTileBytesV + (j + 1 < it.nload ? C::kTileBytesQK : 0));
                 fpar ^= 1u << slot;
                 armed |= 1u << slot;
+                unit_bar = fb;
+  #pragma unroll
+                for (int c = 0; c < C::kChunksV; ++c)
+                  tma_tile(&tm_v, dst + c * C::kChunkBytesV, fb, p.layout, c * C::kChunkElemsV,
+                           hk, j * kBN, it.b, pol_kv);
               }
-#pragma unroll
-              for (int c = 0; c < C::kChunksQK; ++c)
-                tma_tile(&tm_k, dst + c * C::kChunkBytesQK, fb, p.layout,
-                         c * C::kChunkElemsQK, hk, j * kBN, it.b, pol_kv);
-            } else {
-              const uint32_t fb = bar(B::kSlotFull + slot);
-              ptx::mbar_arrive_expect_tx(
-                  fb, C::kTileBytesV + (j + 1 < it.nload ? C::kTileBytesQK : 0));
-              fpar ^= 1u << slot;
-              armed |= 1u << slot;
-              unit_bar = fb;
-#pragma unroll
-              for (int c = 0; c < C::kChunksV; ++c)
-                tma_tile(&tm_v, dst + c * C::kChunkBytesV, fb, p.layout, c * C::kChunkElemsV,
-                         hk, j * kBN, it.b, pol_kv);
+              ++t;
             }
-            ++t;
+          }
+        } else {
+          for (int j = 0; j < it.nload && ok; ++j) {
+            for (int kv = 0; kv < 2; ++kv) {
+              uint32_t base, last;
+              const uint32_t first = ring.place(kv == 1, base, last);
+              if ((own_valid >> last) & 1u) {
+                ok = ptx::mbar_wait(bar(B::kSlotEmpty + ((own_b >> (4 * last)) & 0xFu)),
+                                    (own_par >> last) & 1u, abort, status, 1);
+                if (!ok) break;
+              }
+              const uint32_t rp = (rel_par >> first) & 1u;
+              rel_par ^= 1u << first;
+              for (uint32_t q = first;; q = (q + 1 == NS) ? 0u : q + 1) {
+                own_b = (own_b & ~(0xFu << (4 * q))) | (first << (4 * q));
+                own_par = (own_par & ~(1u << q)) | (rp << q);
+                own_valid |= 1u << q;
+                if (q == last) break;
+              }
+              if (kv == 0) {
+                uint32_t fb = unit_bar;  // K_j, j > 0: second tile of the unit (V_j-1, K_j)
+                if (j == 0) {
+                  fb = bar(B::kSlotFull + first);
+                  ptx::mbar_arrive_expect_tx(fb, C::kTileBytesQK);
+                  fpar ^= 1u << first;
+                  armed |= 1u << first;
+                }
+  #pragma unroll
+                for (int c = 0; c < C::kChunksQK; ++c)
+                  tma_tile(&tm_k, slots_smem + Ring<C>::k_chunk(base, c), fb, p.layout,
+                           c * C::kChunkElemsQK, hk, j * kBN, it.b, pol_kv);
+              } else {
+                const uint32_t fb = bar(B::kSlotFull + first);
+                ptx::mbar_arrive_expect_tx(
+                    fb, C::kTileBytesV + (j + 1 < it.nload ? C::kTileBytesQK : 0));
+                fpar ^= 1u << first;
+                armed |= 1u << first;
+                unit_bar = fb;
+  #pragma unroll
+                for (int c = 0; c < C::kChunksV; ++c)
+                  tma_tile(&tm_v, slots_smem + Ring<C>::v_chunk(base, c), fb, p.layout,
+                           c * C::kChunkElemsV, hk, j * kBN, it.b, pol_kv);
+              }
+            }
           }
         }
       }
       if (!ok) {
         // Unwind: let every copy this thread issued land before the CTA's
         // shared memory is released (each copy completes on the last
-        // arming of some slot's full barrier).
+        // arming of some full barrier).
         for (int x = 0; x < NS; ++x)
           if ((armed >> x) & 1u) ptx::mbar_drain(bar(B::kSlotFull + x), ((fpar >> x) & 1u) ^ 1u);
         for (int s = 0; s < 2; ++s)
@@ -538,8 +653,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t q_par = 0, p_par = 0, pv_par = 0;  // bit s: phase parity per stage
       uint32_t p_count[2] = {0u, 0u};             // P tiles received per stage
-      uint32_t t = 0;
-      uint32_t fpar = 0;  // bit x: phase parity of slot x's full barrier to wait for next
+      uint32_t t = 0;     // slot ring: K/V tiles consumed so far
+      Ring<C> ring;       // chunk-piece ring: placement
+      uint32_t fpar = 0;  // bit x: phase parity of full barrier x to wait for next
       bool ok = true;
       // Base descriptors; an MMA adds its byte offset >> 4 to the start
       // address field (addresses stay below 256 KB, so no carry leaves it).
@@ -547,24 +663,40 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dk0 = ptx::smem_desc(slots_smem, 16, 8 * C::kSwzQK, C::kSwzModeQK);
       const uint64_t dv0 = ptx::smem_desc(slots_smem, C::kChunkBytesV, 1024, 2u);
 
-      // S_s = Q_s K^T from K/V slot `slot`.
-      auto issue_s = [&](int s, uint32_t slot) {
+      // S_s = Q_s K^T, K in slot `kb` (slot ring) or with chunk 0 in piece
+      // `kb` (chunk-piece ring).
+      auto issue_s = [&](int s, uint32_t kb) {
         const uint64_t dq = dq0 + ((s * C::kTileBytesQK) >> 4);
-        const uint64_t dk = dk0 + ((slot * C::kSlotBytes) >> 4);
         const uint32_t d_tmem = tmem + s * 128;
+        if constexpr (!C::kChunkPieces) {
+          const uint64_t dk = dk0 + ((kb * C::kSlotBytes) >> 4);
 #pragma unroll
-        for (int c = 0; c < C::kChunksQK; ++c) {
+          for (int c = 0; c < C::kChunksQK; ++c) {
 #pragma unroll
-          for (int kk = 0; kk < C::kSwzQK / 32; ++kk) {
-            const uint32_t off = (c * C::kChunkBytesQK + kk * 32) >> 4;
-            ptx::mma_ss<C::kF8>(d_tmem, dq + off, dk + off, C::kIdescQK, (c | kk) != 0);
+            for (int kk = 0; kk < C::kSwzQK / 32; ++kk) {
+              const uint32_t off = (c * C::kChunkBytesQK + kk * 32) >> 4;
+              ptx::mma_ss<C::kF8>(d_tmem, dq + off, dk + off, C::kIdescQK, (c | kk) != 0);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < C::kChunksQK; ++c) {
+            const uint64_t dk = dk0 + (Ring<C>::k_chunk(kb, c) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < C::kSwzQK / 32; ++kk) {
+              const uint32_t qoff = (c * C::kChunkBytesQK + kk * 32) >> 4;
+              const uint32_t koff = (kk * 32) >> 4;
+              ptx::mma_ss<C::kF8>(d_tmem, dq + qoff, dk + koff, C::kIdescQK, (c | kk) != 0);
+            }
           }
         }
       };
-      // O_s (+)= P V with V in slot `slot` and P read from tensor memory at
-      // column offset p_col of S_s (FP8 keeps a residual P term at 32).
-      auto issue_pv = [&](int s, uint32_t slot, bool acc_first, uint32_t p_col) {
-        const uint64_t dv = dv0 + ((slot * C::kSlotBytes) >> 4);
+      // O_s (+)= P V, V with chunk 0 in ring piece `vb` (its chunks are
+      // kChunkBytesV apart, the descriptor's leading offset), and P read from
+      // tensor memory at column offset p_col of S_s (FP8 keeps a residual P
+      // term at 32).
+      auto issue_pv = [&](int s, uint32_t vb, bool acc_first, uint32_t p_col) {
+        const uint64_t dv = dv0 + (Ring<C>::v_chunk(vb, 0) >> 4);
         const uint32_t a_tmem = tmem + s * 128 + p_col;
         const uint32_t d_tmem = tmem + 256 + s * 128;
 #pragma unroll
@@ -584,28 +716,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // Prologue: S of K/V tile 0 for both stages.
-        uint32_t slot_k = t % NS;
+        uint32_t kb = 0, kl = 0, slot_k;
+        if constexpr (!C::kChunkPieces) {
+          slot_k = t % NS;
+          ++t;
+          kb = slot_k;
+        } else {
+          slot_k = ring.place(false, kb, kl);
+        }
         ok = ptx::mbar_wait(bar(B::kSlotFull + slot_k), (fpar >> slot_k) & 1u, abort, status, 1);
         if (!ok) break;
         fpar ^= 1u << slot_k;
-        ++t;
         ptx::tc_fence_after();
-        issue_s(0, slot_k);
+        issue_s(0, kb);
         ptx::mma_commit(bar(B::kSFull + 0));
         if (it.n1 > 0) {
-          issue_s(1, slot_k);
+          issue_s(1, kb);
           ptx::mma_commit(bar(B::kSFull + 1));
         }
         ptx::mma_commit(bar(B::kSlotEmpty + slot_k));
 
         for (int j = 0; j < it.nload && ok; ++j) {
           // One wait covers V_j and (when there is a next tile) K_j+1.
-          const uint32_t slot_v = t % NS;
-          ++t;
+          uint32_t vb = 0, vl = 0, slot_v;
+          if constexpr (!C::kChunkPieces) {
+            slot_v = t % NS;
+            ++t;
+            vb = slot_v;
+          } else {
+            slot_v = ring.place(true, vb, vl);
+          }
           const bool has_next = j + 1 < it.nload;
           if (has_next) {
-            slot_k = t % NS;
-            ++t;
+            if constexpr (!C::kChunkPieces) {
+              slot_k = t % NS;
+              ++t;
+              kb = slot_k;
+            } else {
+              slot_k = ring.place(false, kb, kl);
+            }
           }
           ok = ptx::mbar_wait(bar(B::kSlotFull + slot_v), (fpar >> slot_v) & 1u, abort, status, 1);
           if (!ok) break;
@@ -624,8 +773,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // MMA queue would run dry if the issue waited for it.
             uint32_t lo_flag = 0;
             if constexpr (C::kF8) lo_flag = sm.pflag[s];
-            issue_pv(s, slot_v, j > 0, 0);
-            if (C::kF8 && lo_flag == p_count[s]) issue_pv(s, slot_v, true, 32);  // lo term
+            issue_pv(s, vb, j > 0, 0);
+            if (C::kF8 && lo_flag == p_count[s]) issue_pv(s, vb, true, 32);  // lo term
             if (p.serialize_pv && j + 1 < ns) {
               // Verification mode: P (aliasing S) is fully consumed before the
               // next S MMA of this stage overwrites it.
@@ -635,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ok) break;
             }
             if (j + 1 < ns) {
-              issue_s(s, slot_k);
+              issue_s(s, kb);
               ptx::mma_commit(bar(B::kSFull + s));
             } else {
               ptx::mma_commit(bar(B::kOFull + s));
@@ -893,7 +1042,7 @@ static void geometry_of(KernelGeometry* g) {
   g->qk_box_elems = C::kChunkElemsQK;
   g->qk_swizzle = C::kSwzQK;
   g->v_box_elems = C::kChunkElemsV;
-  g->num_slots = C::kNumSlots;
+  g->num_slots = C::kNumPieces;
 }
 
 int kernel_geometry(int dtype, int d_qk, KernelGeometry* g) {
