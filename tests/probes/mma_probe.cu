@@ -8,7 +8,8 @@
 //                operand (the O += P V product).
 //
 // f8 selects kind::f8f6f4 with e4m3 operands instead of kind::f16 with BF16.
-// One CTA of 128 threads; every wait is bounded.
+// One CTA of 128 threads; every wait is bounded.  A second probe lets a
+// bounded wait run out (an arrival that never comes) and reports the status.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -164,9 +165,47 @@ int run(const CUtensorMap& a, const CUtensorMap& b, const void* a_glob, float* d
   return cudaGetLastError();
 }
 
+// Wait-timeout probe: one thread waits on an mbarrier that nothing ever
+// arrives at, with the attention kernel's bounded wait.  out[0] = 1 when the
+// wait (wrongly) reported success, out[1] = the abort flag it raised, out[2]
+// = elapsed global time in microseconds.  The failure is made by withholding
+// the arrival; nothing faults and the wait ends by itself.
+__global__ void wait_timeout_probe_kernel(int* out) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(ptx::smem_u32(&bar), 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = ptx::globaltimer();
+    const bool ok = ptx::mbar_wait(ptx::smem_u32(&bar), 0, &abort_flag, &g_probe_status, 1);
+    out[0] = ok ? 1 : 0;
+    out[1] = abort_flag;
+    out[2] = static_cast<int>((ptx::globaltimer() - t0) / 1000);
+  }
+}
+
 }  // namespace
 
 extern "C" {
+
+// Runs wait_timeout_probe_kernel (one thread; about kWaitTimeoutNs of wall
+// time) and synchronises; out: device, 3 ints.  Returns a cudaError_t.
+__attribute__((visibility("default"))) int zyfa_probe_wait_timeout(int* out) {
+  wait_timeout_probe_kernel<<<1, 32>>>(out);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return cudaDeviceSynchronize();
+}
+
+__attribute__((visibility("default"))) int zyfa_probe_status_reset(void) {
+  const int zero = 0;
+  return cudaMemcpyToSymbol(g_probe_status, &zero, sizeof(int));
+}
+
 
 // a, b: device 128x128 row-major (BF16 or e4m3 codes); d: device FP32 128x128.
 // mode 0: d = a * b^T (both K-major, SS); mode 1: d = a * b (a via TMEM, b MN-major).

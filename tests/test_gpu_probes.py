@@ -54,3 +54,29 @@ def test_probe_mma(probes, f8, mode):
     assert np.all(np.isfinite(got))
     # FP32 accumulation of 128 exact products
     assert err.max() <= 1e-5 * np.abs(ref).max() * 128 ** 0.5 + 1e-6
+
+
+def test_bounded_wait_runs_out_and_reports(probes):
+    """Failure detection without a GPU fault: a wait whose arrival never comes
+    ends after its limit with an error status the host reads, the abort flag
+    raised for the other roles, and the context still usable."""
+    probes.zyfa_probe_wait_timeout.restype = ctypes.c_int
+    probes.zyfa_probe_wait_timeout.argtypes = [ctypes.c_void_p]
+    probes.zyfa_probe_status.restype = ctypes.c_int
+    probes.zyfa_probe_status.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    probes.zyfa_probe_status_reset.restype = ctypes.c_int
+    assert probes.zyfa_probe_status_reset() == 0
+    out = torch.full((3,), -1, dtype=torch.int32, device="cuda")
+    assert probes.zyfa_probe_wait_timeout(out.data_ptr()) == 0
+    ok, aborted, us = out.cpu().tolist()
+    assert ok == 0 and aborted == 1
+    assert 1_000_000 <= us <= 10_000_000      # the 2 s limit, measured on the GPU clock
+    v = ctypes.c_int(0)
+    assert probes.zyfa_probe_status(ctypes.byref(v)) == 0 and v.value & 1
+    assert probes.zyfa_probe_status_reset() == 0
+    # the context is still usable: a small attention call succeeds
+    import causal_flashattention_prefill_gb300 as zf
+    q = torch.randn(1, 300, 2, 128, device="cuda").to(torch.bfloat16)
+    o = zf.flash_attn_func(q, q, q)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o.float()).all()
