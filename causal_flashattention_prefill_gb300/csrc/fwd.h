@@ -38,7 +38,7 @@ struct KernelGeometry {
   int qk_box_elems;    // inner box extent (elements) of Q and K loads
   int qk_swizzle;      // 128 or 64 (bytes)
   int v_box_elems;     // inner box extent of V loads (128-byte swizzle)
-  int num_slots;       // K/V ring slots
+  int num_slots;       // K/V ring entries (whole-tile slots or 16 KB pieces)
 };
 int kernel_geometry(int dtype, int d_qk, KernelGeometry* g);
 

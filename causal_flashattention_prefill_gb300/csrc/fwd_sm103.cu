@@ -15,7 +15,8 @@
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax of stage 0  (thread = query row = TMEM lane)
 //   warps 4-7  softmax of stage 1
-//   warp  8    TMA producer: Q tiles and a ring of K/V tile slots
+//   warp  8    TMA producer: Q tiles and a ring of K/V tiles (whole-tile
+//              slots, or 16 KB pieces for BF16 d_qk = 192)
 //   warp  9    MMA issuer: S = Q K^T (SS form) and O += P V (TS form, P read
 //              from tensor memory, V as an MN-major operand)
 //   warps 10-11 idle (they complete the third warpgroup so that registers
