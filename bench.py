@@ -362,6 +362,24 @@ def oracle_sample(w, budget_s: float = 15.0, t=None):
 
 # ------------------------------------------------------------------ main
 
+def job_mean_ms(local_mean_ms: float, world: int, device) -> float:
+    """Mean step time of the whole job: the slowest rank's (max over ranks,
+    on whatever process group is initialised; the identity on one rank)."""
+    if world <= 1:
+        return local_mean_ms
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([local_mean_ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_tflops(flops_per_rank: float, mean_ms: float, world: int) -> float:
+    """Whole-job TFLOP/s: each of the `world` ranks ran its own problem of
+    `flops_per_rank` within `mean_ms` (weak scaling, no data-path exchange)."""
+    return world * flops_per_rank / (mean_ms * 1e-3) / 1e12
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -438,12 +456,8 @@ def main():
         ms, wall = run_timed(launch, flush, starts, ends, device)
     if world > 1:
         dist.barrier()
-    mean_ms = statistics.mean(ms)
-    if world > 1:
-        tt = torch.tensor([mean_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        mean_ms = float(tt.item())
-    value = world * w.flops / (mean_ms * 1e-3) / 1e12
+    mean_ms = job_mean_ms(statistics.mean(ms), world, device)
+    value = job_tflops(w.flops, mean_ms, world)
     per_gpu = w.flops / (mean_ms * 1e-3) / 1e12
     peak = tensor_peak(w.dtype, peaks)
     traffic = load_traffic(w.name)
