@@ -435,6 +435,44 @@ def dist_setup():
     return world, rank, local
 
 
+def sweep_todo(path: str, names, khash: str) -> list:
+    """Workloads of `names` (in order) that `path` holds no result line for
+    with kernel source hash `khash`; lines that do not parse are ignored."""
+    done = set()
+    if os.path.exists(path):
+        with open(path) as f:
+            for raw in f:
+                try:
+                    d = json.loads(raw)
+                except ValueError:
+                    continue
+                if d.get("kernel_hash") == khash and "workload" in d.get("config", {}):
+                    done.add(d["config"]["workload"])
+    return [n for n in names if n not in done]
+
+
+def run_sweep(path: str, names, steps: int, warmup: int) -> int:
+    """Times each workload in its own process (kernel only, no extra legs)
+    and appends its JSON line to `path`, skipping workloads already recorded
+    for the current kernel source, so an interrupted sweep resumes where it
+    stopped.  Returns the number of workloads that failed."""
+    failed = 0
+    for name in sweep_todo(path, names, kernel_hash()):
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--workload", name,
+                            "--steps", str(steps), "--warmup", str(warmup), "--no-extras"],
+                           capture_output=True, text=True)
+        lines = [x for x in r.stdout.splitlines() if x.startswith("{")]
+        if r.returncode != 0 or not lines:
+            failed += 1
+            print(json.dumps({"workload": name, "failed": r.returncode,
+                              "tail": r.stderr[-400:]}), flush=True)
+            continue
+        with open(path, "a") as f:
+            f.write(lines[-1] + "\n")
+        print(lines[-1], flush=True)
+    return failed
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,7 +482,17 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the e2e, FP8 and CPU-baseline legs")
+    ap.add_argument("--sweep", metavar="FILE",
+                    help="time every workload (or --workloads) into FILE, one JSON line each, "
+                         "resuming after those already recorded for this kernel source")
+    ap.add_argument("--workloads", help="comma-separated workload names for --sweep")
     args = ap.parse_args()
+    if args.sweep:
+        names = args.workloads.split(",") if args.workloads else sorted(workloads.WORKLOADS)
+        for n in names:
+            if n not in workloads.WORKLOADS:
+                raise SystemExit(f"unknown workload {n}")
+        raise SystemExit(1 if run_sweep(args.sweep, names, args.steps, max(3, args.warmup)) else 0)
     warmup = max(3, args.warmup)
     world, rank, local = dist_setup()
     w = workloads.WORKLOADS[args.workload]

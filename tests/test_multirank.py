@@ -64,3 +64,19 @@ def test_reference_arm_runs_on_rank_zero_only():
                         "--steps", "1", "--warmup", "1"], env=env, capture_output=True,
                        text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_sweep_resumes_after_recorded_workloads(tmp_path):
+    path = tmp_path / "sweep.jsonl"
+    h = bench.kernel_hash()
+    lines = [
+        {"config": {"workload": "a"}, "kernel_hash": h},
+        {"config": {"workload": "b"}, "kernel_hash": "other"},   # older kernel: redo
+        "not json",
+        {"config": {"workload": "c"}, "kernel_hash": h},
+    ]
+    with open(path, "w") as f:
+        for x in lines:
+            f.write((x if isinstance(x, str) else __import__("json").dumps(x)) + "\n")
+    assert bench.sweep_todo(str(path), ["a", "b", "c", "d"], h) == ["b", "d"]
+    assert bench.sweep_todo(str(tmp_path / "missing.jsonl"), ["a", "b"], h) == ["a", "b"]
