@@ -520,9 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t q_used = 0;  // bit s: Q buffer s was loaded at least once
       uint32_t t = 0;       // slot ring: K/V tiles issued so far (ring position)
       Ring<C> ring;         // chunk-piece ring: placement
-      // The MMA issuer consumes the tiles in units: K_0 alone, then
-      // (V_j, K_j+1) in step j.  Each unit completes on the full barrier of
-      // its first tile (armed with the bytes of the whole unit), so the
+      // Slot ring: the MMA issuer consumes the tiles in units: K_0 alone,
+      // then (V_j, K_j+1) in step j.  Each unit completes on the full barrier
+      // of its first tile (armed with the bytes of the whole unit), so the
       // issuer waits once per step.  fpar bit x: phase parity of full
       // barrier x after its last arming; armed bit x: armed at least once.
       uint32_t fpar = 0, armed = 0;
@@ -610,25 +610,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 own_valid |= 1u << q;
                 if (q == last) break;
               }
+              // Every tile completes on the full barrier of its first piece,
+              // so the issuer starts P V_j while K_j+1 is still loading.
+              const uint32_t fb = bar(B::kSlotFull + first);
+              ptx::mbar_arrive_expect_tx(fb, kv == 0 ? C::kTileBytesQK : C::kTileBytesV);
+              fpar ^= 1u << first;
+              armed |= 1u << first;
               if (kv == 0) {
-                uint32_t fb = unit_bar;  // K_j, j > 0: second tile of the unit (V_j-1, K_j)
-                if (j == 0) {
-                  fb = bar(B::kSlotFull + first);
-                  ptx::mbar_arrive_expect_tx(fb, C::kTileBytesQK);
-                  fpar ^= 1u << first;
-                  armed |= 1u << first;
-                }
   #pragma unroll
                 for (int c = 0; c < C::kChunksQK; ++c)
                   tma_tile(&tm_k, slots_smem + Ring<C>::k_chunk(base, c), fb, p.layout,
                            c * C::kChunkElemsQK, hk, j * kBN, it.b, pol_kv);
               } else {
-                const uint32_t fb = bar(B::kSlotFull + first);
-                ptx::mbar_arrive_expect_tx(
-                    fb, C::kTileBytesV + (j + 1 < it.nload ? C::kTileBytesQK : 0));
-                fpar ^= 1u << first;
-                armed |= 1u << first;
-                unit_bar = fb;
   #pragma unroll
                 for (int c = 0; c < C::kChunksV; ++c)
                   tma_tile(&tm_v, slots_smem + Ring<C>::v_chunk(base, c), fb, p.layout,
@@ -680,7 +673,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         } else {
-#pragma unroll
+          // Not unrolled over chunks: the smaller issuer code measured up to
+          // 17 % faster on the BF16 d_qk = 192 form (same MMAs, same order).
+#pragma unroll 1
           for (int c = 0; c < C::kChunksQK; ++c) {
             const uint64_t dk = dk0 + (Ring<C>::k_chunk(kb, c) >> 4);
 #pragma unroll
@@ -738,7 +733,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(bar(B::kSlotEmpty + slot_k));
 
         for (int j = 0; j < it.nload && ok; ++j) {
-          // One wait covers V_j and (when there is a next tile) K_j+1.
+          // Slot ring: one wait covers V_j and (when there is a next tile)
+          // K_j+1.
           uint32_t vb = 0, vl = 0, slot_v;
           if constexpr (!C::kChunkPieces) {
             slot_v = t % NS;
@@ -760,6 +756,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = ptx::mbar_wait(bar(B::kSlotFull + slot_v), (fpar >> slot_v) & 1u, abort, status, 1);
           if (!ok) break;
           fpar ^= 1u << slot_v;
+          // Chunk-piece ring: K_j+1 has its own full barrier, waited for
+          // before its first S; V_j is released right after its last P V
+          // (stage 1 when it runs this step), so the pieces it frees start
+          // loading while the last S of the step runs.
+          bool k_pending = C::kChunkPieces && has_next;
+          const int s_last_v = j < it.n1 ? 1 : 0;
           for (int s = 0; s < 2; ++s) {
             const int ns = s == 0 ? it.n0 : it.n1;
             if (j >= ns) continue;
@@ -776,6 +778,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (C::kF8) lo_flag = sm.pflag[s];
             issue_pv(s, vb, j > 0, 0);
             if (C::kF8 && lo_flag == p_count[s]) issue_pv(s, vb, true, 32);  // lo term
+            if constexpr (C::kChunkPieces) {
+              if (s == s_last_v) ptx::mma_commit(bar(B::kSlotEmpty + slot_v));
+            }
             if (p.serialize_pv && j + 1 < ns) {
               // Verification mode: P (aliasing S) is fully consumed before the
               // next S MMA of this stage overwrites it.
@@ -785,6 +790,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!ok) break;
             }
             if (j + 1 < ns) {
+              if constexpr (C::kChunkPieces) {
+                if (k_pending) {
+                  ok = ptx::mbar_wait(bar(B::kSlotFull + slot_k), (fpar >> slot_k) & 1u, abort,
+                                      status, 1);
+                  if (!ok) break;
+                  fpar ^= 1u << slot_k;
+                  k_pending = false;
+                  ptx::tc_fence_after();
+                }
+              }
               issue_s(s, kb);
               ptx::mma_commit(bar(B::kSFull + s));
             } else {
@@ -792,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          ptx::mma_commit(bar(B::kSlotEmpty + slot_v));
+          if constexpr (!C::kChunkPieces) ptx::mma_commit(bar(B::kSlotEmpty + slot_v));
           if (has_next) ptx::mma_commit(bar(B::kSlotEmpty + slot_k));
         }
         if (!ok) break;
