@@ -126,6 +126,13 @@ struct Cfg {
   // Register split: the MMA issuer of the d_qk = 192 BF16 form unrolls 12
   // K steps and needs more registers than the others.
   static constexpr int kSoftmaxRegs = (!kF8 && DQK == 192) ? 184 : 200;
+  // The MMA issuer's loop over the two stages is kept rolled (half the
+  // issuer code) except for BF16 d_qk = 128, where the unrolled loop
+  // measured faster; rolled, the FP8 and d_qk = 192 forms measured 5-12 %
+  // faster on activation-like rows and short sequences.
+  static constexpr bool kRollStages = kF8 || DQK == 192;
+  static_assert(kRollStages || (!kF8 && kSlotsFit >= 3),
+                "the unrolled stage loop carries neither the FP8 residual P V nor the piece ring");
   static constexpr int kOtherRegs = (!kF8 && DQK == 192) ? 136 : 104;
   static_assert(2 * 128 * kSoftmaxRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
@@ -760,50 +767,81 @@ __global__ void __launch_bounds__(kThreads, 1)
           // before its first S; V_j is released right after its last P V
           // (stage 1 when it runs this step), so the pieces it frees start
           // loading while the last S of the step runs.
-          bool k_pending = C::kChunkPieces && has_next;
-          const int s_last_v = j < it.n1 ? 1 : 0;
-          for (int s = 0; s < 2; ++s) {
-            const int ns = s == 0 ? it.n0 : it.n1;
-            if (j >= ns) continue;
-            ok = ptx::mbar_wait(bar(B::kPFull + s), (p_par >> s) & 1u, abort, status, 1);
-            if (!ok) break;
-            p_par ^= 1u << s;
-            ++p_count[s];
-            ptx::tc_fence_after();
-            // The flag is read before the MMAs are issued and used after
-            // them: a shared-memory load from this thread takes hundreds of
-            // cycles while the tensor core streams its operands, and the
-            // MMA queue would run dry if the issue waited for it.
-            uint32_t lo_flag = 0;
-            if constexpr (C::kF8) lo_flag = sm.pflag[s];
-            issue_pv(s, vb, j > 0, 0);
-            if (C::kF8 && lo_flag == p_count[s]) issue_pv(s, vb, true, 32);  // lo term
-            if constexpr (C::kChunkPieces) {
-              if (s == s_last_v) ptx::mma_commit(bar(B::kSlotEmpty + slot_v));
-            }
-            if (p.serialize_pv && j + 1 < ns) {
-              // Verification mode: P (aliasing S) is fully consumed before the
-              // next S MMA of this stage overwrites it.
-              ptx::mma_commit(bar(B::kPvDone + s));
-              ok = ptx::mbar_wait(bar(B::kPvDone + s), (pv_par >> s) & 1u, abort, status, 1);
-              pv_par ^= 1u << s;
-              if (!ok) break;
-            }
-            if (j + 1 < ns) {
+          if constexpr (C::kRollStages) {
+            bool k_pending = C::kChunkPieces && has_next;
+            const int s_last_v = j < it.n1 ? 1 : 0;
+            // One stage's P V and next S.  Returns false when a wait gave up.
+            auto run_stage = [&](int s) -> bool {
+              const int ns = s == 0 ? it.n0 : it.n1;
+              if (j >= ns) return true;
+              ok = ptx::mbar_wait(bar(B::kPFull + s), (p_par >> s) & 1u, abort, status, 1);
+              if (!ok) return false;
+              p_par ^= 1u << s;
+              const uint32_t pcount = s == 0 ? ++p_count[0] : ++p_count[1];
+              ptx::tc_fence_after();
+              // The flag is read before the MMAs are issued and used after
+              // them: a shared-memory load from this thread takes hundreds of
+              // cycles while the tensor core streams its operands, and the
+              // MMA queue would run dry if the issue waited for it.
+              uint32_t lo_flag = 0;
+              if constexpr (C::kF8) lo_flag = sm.pflag[s];
+              issue_pv(s, vb, j > 0, 0);
+              if (C::kF8 && lo_flag == pcount) issue_pv(s, vb, true, 32);  // lo term
               if constexpr (C::kChunkPieces) {
-                if (k_pending) {
-                  ok = ptx::mbar_wait(bar(B::kSlotFull + slot_k), (fpar >> slot_k) & 1u, abort,
-                                      status, 1);
-                  if (!ok) break;
-                  fpar ^= 1u << slot_k;
-                  k_pending = false;
-                  ptx::tc_fence_after();
-                }
+                if (s == s_last_v) ptx::mma_commit(bar(B::kSlotEmpty + slot_v));
               }
-              issue_s(s, kb);
-              ptx::mma_commit(bar(B::kSFull + s));
-            } else {
-              ptx::mma_commit(bar(B::kOFull + s));
+              if (p.serialize_pv && j + 1 < ns) {
+                // Verification mode: P (aliasing S) is fully consumed before the
+                // next S MMA of this stage overwrites it.
+                ptx::mma_commit(bar(B::kPvDone + s));
+                ok = ptx::mbar_wait(bar(B::kPvDone + s), (pv_par >> s) & 1u, abort, status, 1);
+                pv_par ^= 1u << s;
+                if (!ok) return false;
+              }
+              if (j + 1 < ns) {
+                if constexpr (C::kChunkPieces) {
+                  if (k_pending) {
+                    ok = ptx::mbar_wait(bar(B::kSlotFull + slot_k), (fpar >> slot_k) & 1u, abort,
+                                        status, 1);
+                    if (!ok) return false;
+                    fpar ^= 1u << slot_k;
+                    k_pending = false;
+                    ptx::tc_fence_after();
+                  }
+                }
+                issue_s(s, kb);
+                ptx::mma_commit(bar(B::kSFull + s));
+              } else {
+                ptx::mma_commit(bar(B::kOFull + s));
+              }
+              return true;
+            };
+#pragma unroll 1
+            for (int s = 0; s < 2 && ok; ++s) ok = run_stage(s);
+          } else {
+            // BF16 d_qk = 128 (whole-tile slots): the same steps, unrolled
+            // over the two stages.
+            for (int s = 0; s < 2; ++s) {
+              const int ns = s == 0 ? it.n0 : it.n1;
+              if (j >= ns) continue;
+              ok = ptx::mbar_wait(bar(B::kPFull + s), (p_par >> s) & 1u, abort, status, 1);
+              if (!ok) break;
+              p_par ^= 1u << s;
+              ++p_count[s];
+              ptx::tc_fence_after();
+              issue_pv(s, vb, j > 0, 0);
+              if (p.serialize_pv && j + 1 < ns) {
+                ptx::mma_commit(bar(B::kPvDone + s));
+                ok = ptx::mbar_wait(bar(B::kPvDone + s), (pv_par >> s) & 1u, abort, status, 1);
+                pv_par ^= 1u << s;
+                if (!ok) break;
+              }
+              if (j + 1 < ns) {
+                issue_s(s, kb);
+                ptx::mma_commit(bar(B::kSFull + s));
+              } else {
+                ptx::mma_commit(bar(B::kOFull + s));
+              }
             }
           }
           if (!ok) break;
