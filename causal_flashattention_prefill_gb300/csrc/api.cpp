@@ -294,7 +294,7 @@ int zyfa_fp8_quantize_rotated(const void* x, long long n_rows, int d, int x_dtyp
   if (n_rows > (1LL << 40) / d) return ZYFA_ERR_ARG;
   // Tile coordinates of the copies are 32-bit row indices.
   if (n_rows > (1LL << 31) - 1 - zyfa::kRotBoxRows) return ZYFA_ERR_UNSUPPORTED;
-  if (!aligned(x, 16) || !aligned(x8, 8) || !aligned(descale, 4) || !aligned(workspace, 4) ||
+  if (!aligned(x, 16) || !aligned(x8, 16) || !aligned(descale, 4) || !aligned(workspace, 4) ||
       !aligned(signs, 4))
     return ZYFA_ERR_ALIGN;
   const int sms = current_device_sms();

@@ -324,6 +324,16 @@ __device__ __forceinline__ void rot_half(float (&v)[D / 2], const float* s_signs
   }
 }
 
+// Codes are staged in shared memory, eight rows of a warp at a time (16-byte
+// chunk c of row r at chunk rot_code_chunk(c, r) of that row), so that each
+// global store writes 512 contiguous bytes.  The permutation keeps both the
+// per-lane writes (row r, its half of the channels) and the linear read-back
+// free of bank conflicts.
+template <int D>
+__device__ __forceinline__ int rot_code_chunk(int c, int r) {
+  return D == 128 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3));
+}
+
 // The factor of local 32-value block a: 1/sqrt(128) for d = 128; for d = 192
 // the DCT's row norms times 1/8 (H_64 / 8 is orthonormal).
 template <int D>
@@ -377,6 +387,9 @@ __global__ void __launch_bounds__(kRotThreads)
   __shared__ float s_signs[D + 2];
   __shared__ float warp_max[kRotConsumers + 1];
   __shared__ float s_inv;
+  constexpr int kRowChunks = D / 16;               // 16-byte code chunks per row
+  constexpr int kStageChunks = 8 * kRowChunks;     // 8 rows staged per warp at a time
+  __shared__ uint4 s_codes[kQuant ? kRotConsumers * kStageChunks : 1];
   extern __shared__ uint8_t rot_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(rot_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -456,6 +469,9 @@ __global__ void __launch_bounds__(kRotThreads)
       if (!rot_warp_wait(full(st), static_cast<uint32_t>(i / NS) & 1u, abort, lane)) break;
       float v[D / 2];
       rot_read_half<D, XT>(ring + st * T::kTileBytes, r, p, v);
+      // The stage goes back to the tensor copies (async proxy) after these
+      // generic-proxy reads: order them before the release.
+      ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(empty(st));
       // Rows past the end read TMA's zero fill: they rotate to zero and
@@ -470,37 +486,59 @@ __global__ void __launch_bounds__(kRotThreads)
           m = fmaxf(m, mb * rot_scale<D>(a));
         }
       } else {
-        const int64_t row = tile * kRotTileRows + r;
-        if (row < rows) {
-          const float inv = s_inv;
-          const float2 zero = make_float2(0.0f, 0.0f);
-          constexpr int kSeg = RotHalf<D>::kBlock;
+        // Rows past the end are converted too (zeros) but not stored.
+        const float inv = s_inv;
+        const float2 zero = make_float2(0.0f, 0.0f);
+        constexpr int kSeg = RotHalf<D>::kBlock;
+        constexpr int kLaneChunks = D / 32;  // 16-byte code chunks of a half row
+        uint4 oc[kLaneChunks];
 #pragma unroll
-          for (int g = 0; g < (D / 2) / kSeg; ++g) {
-            uint4* dst = reinterpret_cast<uint4*>(x8 + row * D + RotHalf<D>::channel(g * kSeg, p));
+        for (int g = 0; g < (D / 2) / kSeg; ++g) {
 #pragma unroll
-            for (int j = 0; j < kSeg / 16; ++j) {
-              // y = t * (factor * inv) + 0 (adding +0 makes an exactly zero
-              // result +0, whose sign would otherwise follow the order of the
-              // sums, so a zero always gets code 0x00)
-              const int i0 = g * kSeg + 16 * j;
-              const float c = rot_scale<D>(i0 / 32) * inv;
-              const float2 c2 = make_float2(c, c);
-              float y[16];
+          for (int j = 0; j < kSeg / 16; ++j) {
+            // y = t * (factor * inv) + 0 (adding +0 makes an exactly zero
+            // result +0, whose sign would otherwise follow the order of the
+            // sums, so a zero always gets code 0x00)
+            const int i0 = g * kSeg + 16 * j;
+            const float c = rot_scale<D>(i0 / 32) * inv;
+            const float2 c2 = make_float2(c, c);
+            float y[16];
 #pragma unroll
-              for (int q = 0; q < 16; q += 2) {
-                const float2 r = __ffma2_rn(make_float2(v[i0 + q], v[i0 + q + 1]), c2, zero);
-                y[q] = r.x;
-                y[q + 1] = r.y;
-              }
-              uint4 o;
-              o.x = e4m3x4(y[0], y[1], y[2], y[3]);
-              o.y = e4m3x4(y[4], y[5], y[6], y[7]);
-              o.z = e4m3x4(y[8], y[9], y[10], y[11]);
-              o.w = e4m3x4(y[12], y[13], y[14], y[15]);
-              dst[j] = o;
+            for (int q = 0; q < 16; q += 2) {
+              const float2 r = __ffma2_rn(make_float2(v[i0 + q], v[i0 + q + 1]), c2, zero);
+              y[q] = r.x;
+              y[q + 1] = r.y;
+            }
+            uint4& o = oc[i0 / 16];
+            o.x = e4m3x4(y[0], y[1], y[2], y[3]);
+            o.y = e4m3x4(y[4], y[5], y[6], y[7]);
+            o.z = e4m3x4(y[8], y[9], y[10], y[11]);
+            o.w = e4m3x4(y[12], y[13], y[14], y[15]);
+          }
+        }
+        // Two rounds of 8 rows: the lanes of those rows write their chunks,
+        // then the warp stores the rows with 512-byte contiguous writes.
+        uint4* codes = s_codes + warp * kStageChunks;
+        const int rw = lane & 15;  // row within the warp's 16 rows
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if ((rw >> 3) == h) {
+#pragma unroll
+            for (int k = 0; k < kLaneChunks; ++k) {
+              const int chunk = RotHalf<D>::channel(16 * k, p) / 16;  // of local values 16k..
+              codes[(rw & 7) * kRowChunks + rot_code_chunk<D>(chunk, rw & 7)] = oc[k];
             }
           }
+          __syncwarp();
+          const int64_t row0 = tile * kRotTileRows + 16 * warp + 8 * h;
+#pragma unroll
+          for (int k = lane; k < kStageChunks; k += 32) {
+            const int rr = k / kRowChunks, c = k - rr * kRowChunks;
+            if (row0 + rr < rows)
+              reinterpret_cast<uint4*>(x8 + (row0 + rr) * D)[c] =
+                  codes[rr * kRowChunks + rot_code_chunk<D>(c, rr)];
+          }
+          __syncwarp();  // the next round's codes overwrite the buffer
         }
       }
     }

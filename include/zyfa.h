@@ -204,8 +204,10 @@ ZYFA_API int zyfa_fp8_quantize_noalloc(const void* x, long long n, int x_dtype, 
  * d          128 or 192 (others: ZYFA_ERR_UNSUPPORTED).
  * signs      device, d FP32 values, each +1 or -1 (the same for q and k),
  *            4-byte aligned.
- * x8, descale, workspace, stream: as for zyfa_fp8_quantize (x8 holds
- *            n_rows * d codes); deterministic (no atomics).
+ * x8         device, n_rows * d codes, 16-byte aligned (rows are written
+ *            as 16-byte chunks).
+ * descale, workspace, stream: as for zyfa_fp8_quantize; deterministic (no
+ *            atomics).
  * Returns ZYFA_OK or a negative zyfa_status (checks run before any launch).
  */
 ZYFA_API int zyfa_fp8_quantize_rotated(const void* x, long long n_rows, int d, int x_dtype,

@@ -174,6 +174,7 @@ ROT_CASES = [
     (dict(dt=zf.ZYFA_FP8_E4M3), zf.ZYFA_ERR_UNSUPPORTED),
     (dict(x=A + 8), zf.ZYFA_ERR_ALIGN),
     (dict(x8=A + 4), zf.ZYFA_ERR_ALIGN),
+    (dict(x8=A + 8), zf.ZYFA_ERR_ALIGN),   # codes are written as 16-byte chunks
     (dict(signs=A + 2), zf.ZYFA_ERR_ALIGN),
 ]
 

@@ -107,6 +107,28 @@ def test_rotated_quantize_zero_rows():
     assert zf.zyfa_device_status(reset=True) == (zf.ZYFA_OK, 0)
 
 
+@pytest.mark.parametrize("d,rows", [(128, 4099), (192, 1001)])
+def test_rotated_quantize_writes_only_its_rows(d, rows):
+    # Codes are staged in shared memory and stored as whole rows: the call
+    # writes exactly n_rows * d bytes (ragged last tile), equal to the shim's
+    # codes, and leaves the bytes after them untouched.
+    x = (workloads.gaussian((rows, d), 4242 + d) * 3.0).to(torch.bfloat16).cuda()
+    signs = zf.hadamard_signs(d, seed=d)
+    ref8, ref_ds = zf.fp8_quantize_rotated(x, signs)
+    pad = 4096
+    x8 = torch.full((rows * d + pad,), 0xA5, dtype=torch.uint8, device="cuda")
+    ds = torch.zeros(1, dtype=torch.float32, device="cuda")
+    ws = torch.empty(zf.zyfa_fp8_quantize_workspace_bytes(), dtype=torch.uint8, device="cuda")
+    st = zf.zyfa_fp8_quantize_rotated(x.data_ptr(), rows, d, zf.ZYFA_BF16, signs.data_ptr(),
+                                      x8.data_ptr(), ds.data_ptr(), ws.data_ptr(),
+                                      torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert st == zf.ZYFA_OK and zf.zyfa_device_status(reset=True) == (zf.ZYFA_OK, 0)
+    assert float(ds.item()) == float(ref_ds.item())
+    assert torch.equal(x8[: rows * d], ref8.view(torch.uint8).reshape(-1))
+    assert int(x8[rows * d:].min()) == 0xA5 and int(x8[rows * d:].max()) == 0xA5
+
+
 def test_rotated_quantize_activation_like_and_zero():
     # outlier channels (the case rotation is for) and an all-zero tensor
     g = torch.Generator().manual_seed(5)
@@ -123,13 +145,22 @@ def test_rotated_quantize_activation_like_and_zero():
     assert float(zs.item()) == 1.0 and int(z8.view(torch.uint8).max()) == 0
 
 
-def test_rotated_quantize_is_deterministic():
-    x = (workloads.gaussian((20000, 192), 9) * 3.0).to(torch.bfloat16).cuda()
-    s = zf.hadamard_signs(192, seed=3)
+@pytest.mark.parametrize("d,dt,rows", [(128, torch.bfloat16, 524288), (192, torch.bfloat16, 200003),
+                                        (128, torch.float32, 262144), (192, torch.float32, 20000)],
+                         ids=["d128-bf16", "d192-bf16", "d128-f32", "d192-f32"])
+def test_rotated_quantize_is_deterministic(d, dt, rows):
+    # Repeated calls give identical codes.  At 524288 rows of d = 128 BF16
+    # (a four-stage ring of 16 KB tiles) an earlier form of the kernel wrote
+    # a few wrong rows in most calls, which the smaller oracle cases missed.
+    g = torch.Generator(device="cuda").manual_seed(rows + d)
+    x = (torch.randn(rows, d, generator=g, device="cuda") * 3.0).to(dt)
+    s = zf.hadamard_signs(d, seed=3)
     a8, ad = zf.fp8_quantize_rotated(x, s)
-    b8, bd = zf.fp8_quantize_rotated(x, s)
-    torch.cuda.synchronize()
-    assert torch.equal(a8.view(torch.uint8), b8.view(torch.uint8)) and torch.equal(ad, bd)
+    for _ in range(8):
+        b8, bd = zf.fp8_quantize_rotated(x, s)
+        torch.cuda.synchronize()
+        assert torch.equal(a8.view(torch.uint8), b8.view(torch.uint8)) and torch.equal(ad, bd)
+    assert zf.zyfa_device_status(reset=True) == (zf.ZYFA_OK, 0)
 
 
 def _rel_rms(a, b):
