@@ -52,11 +52,17 @@ def test_full_size_sampled_rows(name):
 
 
 @pytest.mark.parametrize("name", ["bf16_gqa_b1_h32kv8_s16384_d128",
-                                  "fp8_gqa_b1_h32kv8_s16384_d128"])
+                                  "fp8_gqa_b1_h32kv8_s16384_d128",
+                                  "bf16_mla_b1_h16_s16384_d192",
+                                  "fp8_mla_b1_h16_s16384_d192"])
 def test_full_size_deterministic(name):
+    # Whole outputs of repeated launches at full size are bitwise equal: a
+    # ring or tensor-memory hazard that strikes a few tiles per launch shows
+    # here even where the sampled rows miss it.  The d_qk = 192 forms cover
+    # both K/V rings (16 KB pieces for BF16, whole-tile slots for FP8).
     w = W[name]
     t = workloads.make_inputs(w)
     O1, L1 = run_gpu(t, w)
-    for _ in range(2):
+    for _ in range(3):
         O2, L2 = run_gpu(t, w)
         assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
