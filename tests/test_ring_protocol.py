@@ -255,9 +255,10 @@ def _simulate_pieces(NP, nK, nV, items, seed, mutate=None):
         acts = []
         if q < len(seq):
             first, last, pieces = placed[q]
+            w = first if mutate == "wait_first_piece" else last
             ok = True
-            if own_valid[last]:
-                ok = empty[own_b[last]].passes(own_par[last])
+            if own_valid[w]:
+                ok = empty[own_b[w]].passes(own_par[w])
             if ok:
                 acts.append("P")
         if run.tma:
@@ -362,4 +363,14 @@ def test_model_catches_reading_k_on_the_v_wait():
     caught = any(_fails(lambda t=t: _simulate_pieces(8, 3, 2, _items(random.Random(t)), t,
                                                      mutate="unit_wait"))
                  for t in range(200))
+    assert caught
+
+
+def test_model_catches_waiting_on_the_first_piece():
+    # The newest earlier owner of a tile's pieces is the owner of its last
+    # piece; waiting on the first piece's owner can let a copy overwrite a
+    # piece still in use (or wait on a stale phase).
+    caught = any(_fails(lambda t=t: _simulate_pieces(8, 3, 2, _items(random.Random(t)), t,
+                                                     mutate="wait_first_piece"))
+                 for t in range(300))
     assert caught
