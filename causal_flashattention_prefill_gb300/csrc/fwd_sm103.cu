@@ -651,7 +651,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the issuing loop (every value in it is
+    // warp-uniform) and one elected lane issues each MMA and commit.
+    {
       uint32_t q_par = 0, p_par = 0, pv_par = 0;  // bit s: phase parity per stage
       uint32_t p_count[2] = {0u, 0u};             // P tiles received per stage
       uint32_t t = 0;     // slot ring: K/V tiles consumed so far
@@ -676,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < C::kSwzQK / 32; ++kk) {
               const uint32_t off = (c * C::kChunkBytesQK + kk * 32) >> 4;
-              ptx::mma_ss<C::kF8>(d_tmem, dq + off, dk + off, C::kIdescQK, (c | kk) != 0);
+              ptx::mma_ss_elect<C::kF8>(d_tmem, dq + off, dk + off, C::kIdescQK, (c | kk) != 0);
             }
           }
         } else {
@@ -689,7 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < C::kSwzQK / 32; ++kk) {
               const uint32_t qoff = (c * C::kChunkBytesQK + kk * 32) >> 4;
               const uint32_t koff = (kk * 32) >> 4;
-              ptx::mma_ss<C::kF8>(d_tmem, dq + qoff, dk + koff, C::kIdescQK, (c | kk) != 0);
+              ptx::mma_ss_elect<C::kF8>(d_tmem, dq + qoff, dk + koff, C::kIdescQK, (c | kk) != 0);
             }
           }
         }
@@ -704,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_tmem = tmem + 256 + s * 128;
 #pragma unroll
         for (int ks = 0; ks < kBN / C::kUmmaK; ++ks)
-          ptx::mma_ts<C::kF8>(d_tmem, a_tmem + ks * 8, dv + ((ks * C::kUmmaK * 128) >> 4),
+          ptx::mma_ts_elect<C::kF8>(d_tmem, a_tmem + ks * 8, dv + ((ks * C::kUmmaK * 128) >> 4),
                               C::kIdescPV, (acc_first || ks > 0) ? 1u : 0u);
       };
 
@@ -714,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = decode_item(w, p);
         const int nst = it.n1 > 0 ? 2 : 1;
         for (int s = 0; s < nst && ok; ++s) {
-          ok = ptx::mbar_wait(bar(B::kQFull + s), (q_par >> s) & 1u, abort, status, 1);
+          ok = warp_wait(bar(B::kQFull + s), (q_par >> s) & 1u, abort, status, lane);
           q_par ^= 1u << s;
         }
         if (!ok) break;
@@ -727,17 +729,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           slot_k = ring.place(false, kb, kl);
         }
-        ok = ptx::mbar_wait(bar(B::kSlotFull + slot_k), (fpar >> slot_k) & 1u, abort, status, 1);
+        ok = warp_wait(bar(B::kSlotFull + slot_k), (fpar >> slot_k) & 1u, abort, status, lane);
         if (!ok) break;
         fpar ^= 1u << slot_k;
         ptx::tc_fence_after();
         issue_s(0, kb);
-        ptx::mma_commit(bar(B::kSFull + 0));
+        ptx::mma_commit_elect(bar(B::kSFull + 0));
         if (it.n1 > 0) {
           issue_s(1, kb);
-          ptx::mma_commit(bar(B::kSFull + 1));
+          ptx::mma_commit_elect(bar(B::kSFull + 1));
         }
-        ptx::mma_commit(bar(B::kSlotEmpty + slot_k));
+        ptx::mma_commit_elect(bar(B::kSlotEmpty + slot_k));
 
         for (int j = 0; j < it.nload && ok; ++j) {
           // Slot ring: one wait covers V_j and (when there is a next tile)
@@ -760,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               slot_k = ring.place(false, kb, kl);
             }
           }
-          ok = ptx::mbar_wait(bar(B::kSlotFull + slot_v), (fpar >> slot_v) & 1u, abort, status, 1);
+          ok = warp_wait(bar(B::kSlotFull + slot_v), (fpar >> slot_v) & 1u, abort, status, lane);
           if (!ok) break;
           fpar ^= 1u << slot_v;
           // Chunk-piece ring: K_j+1 has its own full barrier, waited for
@@ -774,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto run_stage = [&](int s) -> bool {
               const int ns = s == 0 ? it.n0 : it.n1;
               if (j >= ns) return true;
-              ok = ptx::mbar_wait(bar(B::kPFull + s), (p_par >> s) & 1u, abort, status, 1);
+              ok = warp_wait(bar(B::kPFull + s), (p_par >> s) & 1u, abort, status, lane);
               if (!ok) return false;
               p_par ^= 1u << s;
               const uint32_t pcount = s == 0 ? ++p_count[0] : ++p_count[1];
@@ -784,25 +786,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               // cycles while the tensor core streams its operands, and the
               // MMA queue would run dry if the issue waited for it.
               uint32_t lo_flag = 0;
-              if constexpr (C::kF8) lo_flag = sm.pflag[s];
+              if constexpr (C::kF8) lo_flag = __shfl_sync(0xffffffffu, sm.pflag[s], 0);
               issue_pv(s, vb, j > 0, 0);
               if (C::kF8 && lo_flag == pcount) issue_pv(s, vb, true, 32);  // lo term
               if constexpr (C::kChunkPieces) {
-                if (s == s_last_v) ptx::mma_commit(bar(B::kSlotEmpty + slot_v));
+                if (s == s_last_v) ptx::mma_commit_elect(bar(B::kSlotEmpty + slot_v));
               }
               if (p.serialize_pv && j + 1 < ns) {
                 // Verification mode: P (aliasing S) is fully consumed before the
                 // next S MMA of this stage overwrites it.
-                ptx::mma_commit(bar(B::kPvDone + s));
-                ok = ptx::mbar_wait(bar(B::kPvDone + s), (pv_par >> s) & 1u, abort, status, 1);
+                ptx::mma_commit_elect(bar(B::kPvDone + s));
+                ok = warp_wait(bar(B::kPvDone + s), (pv_par >> s) & 1u, abort, status, lane);
                 pv_par ^= 1u << s;
                 if (!ok) return false;
               }
               if (j + 1 < ns) {
                 if constexpr (C::kChunkPieces) {
                   if (k_pending) {
-                    ok = ptx::mbar_wait(bar(B::kSlotFull + slot_k), (fpar >> slot_k) & 1u, abort,
-                                        status, 1);
+                    ok = warp_wait(bar(B::kSlotFull + slot_k), (fpar >> slot_k) & 1u, abort,
+                                        status, lane);
                     if (!ok) return false;
                     fpar ^= 1u << slot_k;
                     k_pending = false;
@@ -810,9 +812,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   }
                 }
                 issue_s(s, kb);
-                ptx::mma_commit(bar(B::kSFull + s));
+                ptx::mma_commit_elect(bar(B::kSFull + s));
               } else {
-                ptx::mma_commit(bar(B::kOFull + s));
+                ptx::mma_commit_elect(bar(B::kOFull + s));
               }
               return true;
             };
@@ -824,35 +826,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < 2; ++s) {
               const int ns = s == 0 ? it.n0 : it.n1;
               if (j >= ns) continue;
-              ok = ptx::mbar_wait(bar(B::kPFull + s), (p_par >> s) & 1u, abort, status, 1);
+              ok = warp_wait(bar(B::kPFull + s), (p_par >> s) & 1u, abort, status, lane);
               if (!ok) break;
               p_par ^= 1u << s;
               ++p_count[s];
               ptx::tc_fence_after();
               issue_pv(s, vb, j > 0, 0);
               if (p.serialize_pv && j + 1 < ns) {
-                ptx::mma_commit(bar(B::kPvDone + s));
-                ok = ptx::mbar_wait(bar(B::kPvDone + s), (pv_par >> s) & 1u, abort, status, 1);
+                ptx::mma_commit_elect(bar(B::kPvDone + s));
+                ok = warp_wait(bar(B::kPvDone + s), (pv_par >> s) & 1u, abort, status, lane);
                 pv_par ^= 1u << s;
                 if (!ok) break;
               }
               if (j + 1 < ns) {
                 issue_s(s, kb);
-                ptx::mma_commit(bar(B::kSFull + s));
+                ptx::mma_commit_elect(bar(B::kSFull + s));
               } else {
-                ptx::mma_commit(bar(B::kOFull + s));
+                ptx::mma_commit_elect(bar(B::kOFull + s));
               }
             }
           }
           if (!ok) break;
-          if constexpr (!C::kChunkPieces) ptx::mma_commit(bar(B::kSlotEmpty + slot_v));
-          if (has_next) ptx::mma_commit(bar(B::kSlotEmpty + slot_k));
+          if constexpr (!C::kChunkPieces) ptx::mma_commit_elect(bar(B::kSlotEmpty + slot_v));
+          if (has_next) ptx::mma_commit_elect(bar(B::kSlotEmpty + slot_k));
         }
         if (!ok) break;
-        for (int s = 0; s < nst; ++s) ptx::mma_commit(bar(B::kQEmpty + s));
+        for (int s = 0; s < nst; ++s) ptx::mma_commit_elect(bar(B::kQEmpty + s));
       }
       // Every MMA this thread issued completes before tensor memory is freed.
-      ptx::mma_commit(bar(B::kDrain));
+      ptx::mma_commit_elect(bar(B::kDrain));
       ptx::mbar_drain(bar(B::kDrain), 0);
     }
     __syncwarp();
@@ -1023,7 +1025,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) ptx::mbar_arrive(bar(B::kPFull + s));
       }
       if (!ok) break;
-      // Epilogue: O / l (times v_descale and 2^-8 for FP8), BF16, and LSE.
+      // Epilogue: O * v_descale / lr as BF16 (FP8: the 2^4 pre-scale of P
+      // cancels, lr summing the same pre-scaled values), and the LSE.
       ok = warp_wait(bar(B::kOFull + s), o_uses & 1u, abort, status, lane);
       if (!ok) break;
       ++o_uses;
