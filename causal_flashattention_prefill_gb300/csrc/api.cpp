@@ -277,11 +277,9 @@ int zyfa_fp8_quantize_noalloc(const void* x, long long n, int x_dtype, void* x8,
   if (!aligned(x, 16) || !aligned(x8, 8) || !aligned(descale, 4)) return ZYFA_ERR_ALIGN;
   const int sms = current_device_sms();
   if (sms <= 0) return ZYFA_ERR_DEVICE;
-  int too_large = 0;
   const int e = zyfa::fp8_quantize_noalloc(
       x, n, x_dtype == ZYFA_BF16 ? zyfa::kQuantBF16 : zyfa::kQuantF32, x8, descale, sms,
-      reinterpret_cast<cudaStream_t>(stream), &too_large);
-  if (too_large) return ZYFA_ERR_UNSUPPORTED;
+      reinterpret_cast<cudaStream_t>(stream));
   return e == 0 ? ZYFA_OK : ZYFA_ERR_LAUNCH;
 }
 

@@ -1,8 +1,8 @@
 // Per-tensor FP8 e4m3 quantisation with a power-of-two descale: the input
 // preparation step of the FP8 path (ZYFA README, "Usage": fp8_quantize
 // returns the e4m3 tensor and one power-of-two descale per tensor, as a GPU
-// scalar so that no call waits for the host; "Kernel design": every
-// conversion rounds to nearest even).
+// scalar so that no call waits for the host; "Kernel design": all format
+// conversions use round-half-to-even).
 //
 // descale = smallest power of two with max|x| / descale <= 448 (1 for an
 // all-zero tensor); x8 = e4m3_rne_satfinite(x / descale).
@@ -633,6 +633,11 @@ namespace zyfa {
 namespace {
 
 static __device__ __align__(256) float g_noalloc_partials[kQuantMaxPartials];
+// The first pass launches at most kQuantMaxPartials CTAs (launch_t and
+// launch_rot_t clamp their grids to it) and writes one maximum per CTA, so
+// every input size fits the array.
+static_assert(sizeof(g_noalloc_partials) / sizeof(float) >= kQuantMaxPartials,
+              "the array holds one maximum per CTA of the largest first pass");
 
 constexpr int kMaxDevicesNoAlloc = 64;
 std::mutex g_noalloc_mu;
@@ -641,8 +646,7 @@ float* g_noalloc_ptr[kMaxDevicesNoAlloc] = {};
 }  // namespace
 
 int fp8_quantize_noalloc(const void* x, int64_t n, int x_type, void* x8, float* descale, int sms,
-                         cudaStream_t stream, int* too_large) {
-  *too_large = 0;
+                         cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -651,6 +655,8 @@ int fp8_quantize_noalloc(const void* x, int64_t n, int x_type, void* x8, float* 
   {
     // One-time set-up per device, with that device current: host code needs
     // the array's device address (its name is only a host-side stand-in).
+    // The address is kept for the life of the process, so the entry point is
+    // not usable on a device after cudaDeviceReset there.
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     if (!g_noalloc_ptr[dev]) {
       void* p = nullptr;
@@ -659,14 +665,6 @@ int fp8_quantize_noalloc(const void* x, int64_t n, int x_type, void* x8, float* 
       g_noalloc_ptr[dev] = static_cast<float*>(p);
     }
     partials = g_noalloc_ptr[dev];
-  }
-  // The first pass writes one maximum per CTA and launches at most
-  // min(kQuantMaxPartials, 4 * SMs) CTAs; reject a device whose first pass
-  // would need more slots than the array holds.
-  const int slots = kQuantMaxPartials < 4 * sms ? kQuantMaxPartials : 4 * sms;
-  if (slots > static_cast<int>(sizeof(g_noalloc_partials) / sizeof(float))) {
-    *too_large = 1;
-    return cudaErrorInvalidValue;
   }
   // Nothing needs clearing: the second pass reads only the slots the first
   // pass of the same call has written.

@@ -31,9 +31,8 @@ constexpr int kRotBoxRows = 64;
 int read_rot_status(int* value, int reset);
 
 // Same, with the first pass's maxima in a file-scope device array instead of a
-// caller workspace (one-time symbol lookup per device on first use).  Sets
-// *too_large when the array cannot hold the first pass's maxima.
+// caller workspace (one-time symbol lookup per device on first use).
 int fp8_quantize_noalloc(const void* x, int64_t n, int x_type, void* x8, float* descale, int sms,
-                         cudaStream_t stream, int* too_large);
+                         cudaStream_t stream);
 
 }  // namespace zyfa

@@ -8,12 +8,12 @@
  *   LSE[b, h, i]  = ln sum_{j <= i} exp(scale * <q[b,i,h], k[b,j,hk]>)
  *
  * with seqlen_q = seqlen_k = S, equal-length batches, hk = h / (H / Hkv)
- * (MHA, GQA and MQA: "nheads a multiple of nheads_k"), head dims
- * d_qk = d_v = 128 or d_qk = 192 with d_v = 128, BF16 or FP8 e4m3 inputs with
- * one descale per tensor (applied by the kernel from device memory; "Usage":
- * "The kernel reads tensor descales from GPU memory and applies all three
- * itself"), BF16 output and an optional FP32 natural-log LSE of the scaled
- * scores.  Any S >= 1 is accepted: lengths that are not a multiple of the tile
+ * (MHA, GQA and MQA: the query-head count is any multiple of the KV-head
+ * count), head dims d_qk = d_v = 128 or d_qk = 192 with d_v = 128, BF16 or
+ * FP8 e4m3 inputs with one descale per tensor (the kernel itself loads the
+ * three descales from device memory and applies them, so no call waits for
+ * the host; "Usage"), BF16 output and an optional FP32 natural-log LSE of the
+ * scaled scores.  Any S >= 1 is accepted: lengths that are not a multiple of the tile
  * give the same result as zero-padding ("Usage": padding is exact for causal
  * attention), with no copy.
  *
@@ -85,22 +85,40 @@ ZYFA_API int zyfa_fwd(const void* q, const void* k, const void* v, void* out, fl
              const float* k_descale, const float* v_descale, int layout,
              struct CUstream_st* stream);
 
-/* Same as zyfa_fwd with an explicit softmax_scale (finite, > 0). */
+/*
+ * zyfa_fwd with an explicit softmax_scale (finite, > 0): the scale argument of
+ * flash_attn_func in the ZYFA README ("Usage"; "Differences from flash-attn":
+ * the flash-attn calling convention, scale default 1/sqrt(head dim)).  The
+ * scale multiplies the scores before the softmax and enters the LSE; for FP8
+ * inputs it is applied on top of q_descale * k_descale.  Other arguments,
+ * ownership and errors as zyfa_fwd (a scale that is not finite and positive
+ * returns ZYFA_ERR_ARG before any CUDA call).
+ */
 ZYFA_API int zyfa_fwd_scaled(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                     int S, int H, int Hkv, int d_qk, int d_v, int dtype, const float* q_descale,
                     const float* k_descale, const float* v_descale, float softmax_scale,
                     int layout, struct CUstream_st* stream);
 
 /*
- * Runs only the host-side argument checks of zyfa_fwd_scaled (no CUDA call).
- * Returns ZYFA_OK when zyfa_fwd_scaled would launch.
+ * Runs only the host-side argument checks of zyfa_fwd_scaled, with no CUDA
+ * call (the supported configurations of the ZYFA README, "Supported
+ * configurations": causal, seqlen_q = seqlen_k, head dims (128, 128) or
+ * (192, 128), query heads a multiple of KV heads, BF16 or FP8 e4m3 inputs;
+ * "Usage": FP8 needs all three descales).  Pointers are only checked for
+ * NULL and alignment, never dereferenced.  Returns ZYFA_OK when
+ * zyfa_fwd_scaled would launch, else the status that call would return.
  */
 ZYFA_API int zyfa_validate(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                   int S, int H, int Hkv, int d_qk, int d_v, int dtype, const float* q_descale,
                   const float* k_descale, const float* v_descale, float softmax_scale,
                   int layout);
 
-/* Static description of a status code; never NULL. */
+/*
+ * Static English description of a zyfa_status value (unknown values give
+ * "unknown status"); never NULL, owned by the library.  The statuses are how
+ * this C interface reports the rejections the ZYFA README lists under
+ * "Supported configurations" (ZYFA_ERR_UNSUPPORTED) and invalid arguments.
+ */
 ZYFA_API const char* zyfa_status_string(int status);
 
 /*
@@ -125,8 +143,8 @@ ZYFA_API int zyfa_set_option(int option, int value);
 /*
  * Per-tensor FP8 quantisation (the input preparation of the FP8 path; ZYFA
  * README, "Usage": fp8_quantize returns the e4m3 tensor and one power-of-two
- * descale per tensor as a GPU scalar; "Kernel design": conversions round to
- * nearest even).
+ * descale per tensor as a GPU scalar; "Kernel design": all conversions use
+ * round-half-to-even).
  *
  *   descale = smallest power of two with max|x| / descale <= 448 (1 if x is
  *             all zero);   x8[i] = e4m3(x[i] / descale), ties to even,
@@ -162,14 +180,16 @@ ZYFA_API long long zyfa_fp8_quantize_workspace_bytes(void);
  * `workspace`.  The scratch it needs (one FP32 maximum per CTA of the first
  * pass, at most 1024 of them) lives in a 4 KB array inside this library,
  * kept on every device that runs this entry point until the process exits.
- * A request whose first pass would need more than those 1024 slots is
- * rejected with ZYFA_ERR_UNSUPPORTED (this device's first pass uses at most
- * four per SM).  Nothing in the array has to start at zero, but all calls on
- * a device share it, so calls that may run at the same time on the GPU (on
- * different streams without ordering) race and must not be made.  The first
- * call on each device looks up the array's device address (a CUDA runtime
- * call) and should come before any stream capture.  The entry point never
- * allocates: no cudaMalloc, no cudaFree, no allocating library routine.
+ * The first pass never launches more CTAs than the array has slots, so every
+ * input size fits.  Nothing in the array has to start at zero, but all calls
+ * on a device share it, so calls that may run at the same time on the GPU
+ * (on different streams without ordering) race and must not be made.  The
+ * first call on each device looks up the array's device address (a CUDA
+ * runtime call) and should come before any stream capture; the address is
+ * kept for the life of the process, so after cudaDeviceReset on a device
+ * this entry point must not be called on that device again.  The entry
+ * point never allocates: no cudaMalloc, no cudaFree, no allocating library
+ * routine.
  */
 ZYFA_API int zyfa_fp8_quantize_noalloc(const void* x, long long n, int x_dtype, void* x8,
                                        float* descale, struct CUstream_st* stream);

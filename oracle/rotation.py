@@ -7,9 +7,9 @@ R = diag(s) H / sqrt(d) with H the d x d Hadamard matrix of Sylvester's
 construction (H_1 = [1], H_2n = [[H_n, H_n], [H_n, -H_n]]) and s a vector of
 random signs, applied to each head row as x @ R (after RoPE; v is left
 unrotated).  R is orthogonal, so (qR)(kR)^T = qk^T and only the rounding of
-the quantised inputs changes.  For d = 192, which is not a power of two, the
-README combines a 3-point discrete cosine transform with a 64-point Hadamard
-matrix; the reading taken here is the Kronecker product
+the quantised inputs changes.  A 192-channel head has no Hadamard matrix of
+its own size, so there the README mixes a DCT of length 3 with a Hadamard
+matrix of order 64; the reading taken here is the Kronecker product
 R = diag(s) (C3^T kron H_64) / 8, with C3 the orthonormal DCT-II matrix
 C3[k, n] = a_k cos(pi (2n + 1) k / 6), a_0 = sqrt(1/3), a_k = sqrt(2/3):
 row block n of x (columns 64n .. 64n+63) is transformed by H_64 / 8 and the
