@@ -9,7 +9,6 @@ from flash-attn") and reach the library through the custom operator
 
 from __future__ import annotations
 
-import math
 from typing import Optional, Tuple
 
 import torch
@@ -39,12 +38,14 @@ def _ptr(t):
 
 def attention(q, k, v, out=None, lse=None, q_descale=None, k_descale=None, v_descale=None,
               softmax_scale=None, layout="bshd", return_lse=False, stream=None):
-    """Causal forward attention on device tensors through ``zyfa_fwd_scaled``.
+    """Causal forward attention on device tensors through the C ABI.
 
     ``q`` (B,S,H,d_qk) and ``k``/``v`` (B,S,Hkv,d) for ``layout="bshd"``, or
     (B,H,S,d) for ``"bhsd"``; BF16 or float8_e4m3fn, contiguous.  FP8 needs
     three 1-element float32 device descale tensors.  ``out``/``lse`` are
-    allocated when not given.  Returns ``out`` or ``(out, lse)``.
+    allocated when not given.  Without ``softmax_scale`` the call goes to
+    ``zyfa_fwd``, which applies the default scale itself; with one, to
+    ``zyfa_fwd_scaled``.  Returns ``out`` or ``(out, lse)``.
     """
     dt = _dtype_code(q)
     if not (k.dtype == q.dtype and v.dtype == q.dtype):
@@ -67,13 +68,14 @@ def attention(q, k, v, out=None, lse=None, q_descale=None, k_descale=None, v_des
         out = torch.empty(out_shape, dtype=torch.bfloat16, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty((B, H, S), dtype=torch.float32, device=q.device)
-    if softmax_scale is None:
-        softmax_scale = 1.0 / math.sqrt(d_qk)
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
-    st = _lib.zyfa_fwd_scaled(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, Hkv,
-                              d_qk, d_v, dt, _ptr(q_descale), _ptr(k_descale), _ptr(v_descale),
-                              float(softmax_scale), lay, stream)
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, S, H, Hkv, d_qk, d_v, dt,
+            _ptr(q_descale), _ptr(k_descale), _ptr(v_descale))
+    if softmax_scale is None:
+        st = _lib.zyfa_fwd(*args, lay, stream)
+    else:
+        st = _lib.zyfa_fwd_scaled(*args, float(softmax_scale), lay, stream)
     if st != _lib.ZYFA_OK:
         raise ZyfaError(st)
     return (out, lse) if return_lse else out
@@ -127,7 +129,7 @@ def _descale_tensor(d, device):
 @torch.library.custom_op("zyfa::fwd", mutates_args=())
 def _fwd_op(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor,
             q_descale: Optional[torch.Tensor], k_descale: Optional[torch.Tensor],
-            v_descale: Optional[torch.Tensor], softmax_scale: float, layout: str,
+            v_descale: Optional[torch.Tensor], softmax_scale: Optional[float], layout: str,
             return_lse: bool) -> Tuple[torch.Tensor, torch.Tensor]:
     res = attention(q, k, v, q_descale=q_descale, k_descale=k_descale, v_descale=v_descale,
                     softmax_scale=softmax_scale, layout=layout, return_lse=return_lse)
@@ -179,10 +181,10 @@ def flash_attn_func(q, k, v, dropout_p=0.0, softmax_scale=None, causal=True,
         raise ValueError(f"layout is 'bshd' or 'bhsd', not {layout!r}")
     q, k, v = (t.contiguous() for t in (q, k, v))
     dq, dk, dv = (_descale_tensor(d, q.device) for d in (q_descale, k_descale, v_descale))
-    if softmax_scale is None:
-        softmax_scale = 1.0 / math.sqrt(q.shape[-1])
+    if softmax_scale is not None:
+        softmax_scale = float(softmax_scale)
     want_lse = bool(return_lse or return_attn_probs)
-    out, lse = torch.ops.zyfa.fwd(q, k, v, dq, dk, dv, float(softmax_scale), layout, want_lse)
+    out, lse = torch.ops.zyfa.fwd(q, k, v, dq, dk, dv, softmax_scale, layout, want_lse)
     if not want_lse:
         lse = None
     if return_attn_probs:
