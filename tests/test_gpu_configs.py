@@ -13,6 +13,7 @@ import numpy as np
 import pytest
 import torch
 
+import causal_flashattention_prefill_gb300 as zf
 import workloads
 from gpu_util import assert_parity, run_gpu, run_oracle
 
@@ -31,9 +32,19 @@ FULL = [
      for S in (2048, 4096, 16384, 30000, 32768)]
 
 
+# The spec shapes (the S = 16384 GQA workloads and both MLA forms) are
+# checked on every head; the two-batch MHA sweep, whose oracle would cost
+# minutes per workload on all heads, on three heads per batch.
+ALL_HEADS = {"fp8_gqa_b1_h32kv8_s16384_d128", "bf16_gqa_b1_h32kv8_s16384_d128",
+             "bf16_mla_b1_h16_s16384_d192", "fp8_mla_b1_h16_s16384_d192",
+             "bf16_mha_b1_h2_s256_d128"}
+
+
 def _heads(w):
-    """(batch, head) pairs to check: first, last, and one from the middle of
-    a KV group, in every batch."""
+    """Heads to check in every batch: all of them for ALL_HEADS, else the
+    first, the last and one from the middle of a KV group."""
+    if w.name in ALL_HEADS:
+        return list(range(w.H))
     hs = sorted({0, w.H - 1, min(w.H - 1, w.H // 2 + 1)})
     return hs
 
@@ -60,9 +71,80 @@ def test_full_size_deterministic(name):
     # ring or tensor-memory hazard that strikes a few tiles per launch shows
     # here even where the sampled rows miss it.  The d_qk = 192 forms cover
     # both K/V rings (16 KB pieces for BF16, whole-tile slots for FP8).
+    # Launches 3 and 4 run with a BF16 GEMM between them, the second one
+    # with the GEMM on another stream running alongside the attention: the
+    # ZYFA README ("Accuracy") contrasts its launch-to-launch identical
+    # outputs with a library whose results change when a GEMM runs between
+    # launches, and here neither order nor a concurrent kernel may change a bit.
     w = W[name]
     t = workloads.make_inputs(w)
     O1, L1 = run_gpu(t, w)
-    for _ in range(3):
-        O2, L2 = run_gpu(t, w)
-        assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+    O2, L2 = run_gpu(t, w)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+    a = torch.randn(8192, 8192, device="cuda", dtype=torch.bfloat16)
+    side = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    c = a @ a                                  # between launches, same stream
+    O3, L3 = run_gpu(t, w)
+    assert np.array_equal(O1, O3) and np.array_equal(L1, L3)
+    with torch.cuda.stream(side):              # alongside the next launch
+        for _ in range(8):
+            c = a @ a
+    O4, L4 = run_gpu(t, w)
+    side.synchronize()
+    assert np.array_equal(O1, O4) and np.array_equal(L1, L4)
+    del a, c
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+@pytest.mark.parametrize("d_qk,layout", [(128, "bshd"), (192, "bhsd")])
+def test_multi_item_ctas_every_element(dtype, d_qk, layout):
+    # 2 batches x 16 heads x 16 query blocks = 512 work items over at most
+    # one CTA per SM: every CTA runs three or four items in a row, so the
+    # ring and barrier bookkeeping that carries from one item to the next,
+    # tensor-memory reuse and the Q-buffer hand-over are all compared with
+    # the oracle element by element.
+    w = workloads.Workload("multi_item", dtype, 2, 4096, 16, 4, d_qk=d_qk, d_v=128,
+                           layout=layout, seed=5200 + d_qk + (dtype == "fp8"))
+    n_items = w.B * w.H * ((w.S + 255) // 256)
+    assert n_items > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    t = workloads.make_inputs(w)
+    O, L = run_gpu(t, w)
+    Oref, Lref = run_oracle(t, w)
+    assert_parity(O, L, Oref, Lref, dtype, f"multi-item {dtype} d{d_qk} {layout}")
+
+
+def test_tensor_beyond_32bit_element_offsets():
+    # q and out hold 17 * 32768 * 32 * 128 > 2^31 elements (4.6 GB each in
+    # BF16): every element of batch 16 sits past element 2^31 and past byte
+    # 2^32, so a 32-bit element or byte offset anywhere on the path (tensor
+    # maps, output and LSE addressing) would read or write another batch.
+    # Each batch has its own seeded draw, so such a mix-up changes values.
+    # Checked on sampled rows of two heads in the first and last batch.
+    w = workloads.Workload("big", "bf16", 17, 32768, 32, 8, seed=6100)
+    assert w.B * w.S * w.H * w.d_qk > 2 ** 31
+    dev = torch.device("cuda")
+    q = torch.empty((w.B, w.S, w.H, w.d_qk), dtype=torch.bfloat16, device=dev)
+    k = torch.empty((w.B, w.S, w.Hkv, w.d_qk), dtype=torch.bfloat16, device=dev)
+    v = torch.empty((w.B, w.S, w.Hkv, w.d_v), dtype=torch.bfloat16, device=dev)
+    for b in range(w.B):
+        q[b].copy_(workloads.gaussian(q.shape[1:], w.seed + 10 * b).to(torch.bfloat16))
+        k[b].copy_(workloads.gaussian(k.shape[1:], w.seed + 10 * b + 1).to(torch.bfloat16))
+        v[b].copy_(workloads.gaussian(v.shape[1:], w.seed + 10 * b + 2).to(torch.bfloat16))
+    out, lse = zf.attention(q, k, v, return_lse=True)
+    torch.cuda.synchronize()
+    rows = workloads.sample_rows(w.S, seed=w.seed, n_random=128)
+    heads = [0, w.H - 1]
+    r = torch.as_tensor(rows, device=dev)
+    for b in (0, w.B - 1):
+        tb = dict(q=q[b:b + 1].cpu(), k=k[b:b + 1].cpu(), v=v[b:b + 1].cpu(),
+                  q_descale=1.0, k_descale=1.0, v_descale=1.0)
+        wb = w.with_(B=1)
+        Oref, Lref = run_oracle(tb, wb, rows=rows, heads=heads)
+        h = torch.as_tensor(heads, device=dev)
+        Og = out[b:b + 1].index_select(1, r).index_select(2, h).transpose(1, 2)
+        Lg = lse[b:b + 1].index_select(1, h).index_select(2, r)
+        assert_parity(Og.float().cpu().double().numpy(), Lg.cpu().double().numpy(), Oref, Lref,
+                      "bf16", f"beyond 2^31 elements, batch {b}")
+    del q, k, v, out, lse
+    torch.cuda.empty_cache()
