@@ -51,10 +51,11 @@ EncodeTiledFn encode_fn() {
 }
 
 // Returns the SM count of the current device, or -1 when it is not an
-// sm_103 device.
-int current_device_sms() {
+// sm_103 device; *device_out (optional) receives the device index.
+int current_device_sms(int* device_out = nullptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  if (device_out) *device_out = dev;
   std::lock_guard<std::mutex> lk(g_mu);
   DeviceInfo& d = g_dev[dev];
   if (d.checked == 0) {
@@ -69,6 +70,50 @@ int current_device_sms() {
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Tensor maps of recent calls, keyed by everything they encode (base
+// addresses, sizes, layout, element type; the box geometry follows from
+// dtype and d_qk).  A map holds no device state, so an entry stays valid
+// whatever happens to the buffers; repeated calls on the same buffers skip
+// the three encodings.
+struct MapKey {
+  const void* q;
+  const void* k;
+  const void* v;
+  int dtype, layout, B, S, H, Hkv, d_qk, d_v;
+  bool operator==(const MapKey& o) const {
+    return q == o.q && k == o.k && v == o.v && dtype == o.dtype && layout == o.layout &&
+           B == o.B && S == o.S && H == o.H && Hkv == o.Hkv && d_qk == o.d_qk && d_v == o.d_v;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  zyfa::TensorMaps maps;
+  bool valid = false;
+};
+constexpr int kMapCacheEntries = 16;
+MapEntry g_map_cache[kMapCacheEntries];
+int g_map_cache_next = 0;
+
+bool cached_maps(const MapKey& key, zyfa::TensorMaps* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (const MapEntry& e : g_map_cache) {
+    if (e.valid && e.key == key) {
+      *out = e.maps;
+      return true;
+    }
+  }
+  return false;
+}
+
+void remember_maps(const MapKey& key, const zyfa::TensorMaps& maps) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  MapEntry& e = g_map_cache[g_map_cache_next];
+  g_map_cache_next = (g_map_cache_next + 1) % kMapCacheEntries;
+  e.key = key;
+  e.maps = maps;
+  e.valid = true;
+}
 
 int validate(const void* q, const void* k, const void* v, void* out, float* lse, int B, int S,
              int H, int Hkv, int d_qk, int d_v, int dtype, const float* q_descale,
@@ -174,18 +219,23 @@ int zyfa_fwd_scaled(const void* q, const void* k, const void* v, void* out, floa
   int st = validate(q, k, v, out, lse, B, S, H, Hkv, d_qk, d_v, dtype, q_descale, k_descale,
                     v_descale, softmax_scale, layout);
   if (st != ZYFA_OK) return st;
-  const int sms = current_device_sms();
+  int device = 0;
+  const int sms = current_device_sms(&device);
   if (sms <= 0) return ZYFA_ERR_DEVICE;
 
   zyfa::KernelGeometry g;
   if (zyfa::kernel_geometry(dtype, d_qk, &g) != 0) return ZYFA_ERR_UNSUPPORTED;
   zyfa::TensorMaps maps;
-  std::memset(&maps, 0, sizeof(maps));
-  if ((st = make_map(&maps.q, q, dtype, layout, B, S, H, d_qk, g.qk_box_elems, g.qk_swizzle)))
-    return st;
-  if ((st = make_map(&maps.k, k, dtype, layout, B, S, Hkv, d_qk, g.qk_box_elems, g.qk_swizzle)))
-    return st;
-  if ((st = make_map(&maps.v, v, dtype, layout, B, S, Hkv, d_v, g.v_box_elems, 128))) return st;
+  const MapKey key{q, k, v, dtype, layout, B, S, H, Hkv, d_qk, d_v};
+  if (!cached_maps(key, &maps)) {
+    std::memset(&maps, 0, sizeof(maps));
+    if ((st = make_map(&maps.q, q, dtype, layout, B, S, H, d_qk, g.qk_box_elems, g.qk_swizzle)))
+      return st;
+    if ((st = make_map(&maps.k, k, dtype, layout, B, S, Hkv, d_qk, g.qk_box_elems, g.qk_swizzle)))
+      return st;
+    if ((st = make_map(&maps.v, v, dtype, layout, B, S, Hkv, d_v, g.v_box_elems, 128))) return st;
+    remember_maps(key, maps);
+  }
 
   zyfa::FwdParams p;
   std::memset(&p, 0, sizeof(p));
@@ -206,7 +256,8 @@ int zyfa_fwd_scaled(const void* q, const void* k, const void* v, void* out, floa
   p.serialize_pv = g_serialize_pv.load(std::memory_order_relaxed);
   p.softmax_scale = softmax_scale;
   const int grid = p.total_items < sms ? p.total_items : sms;
-  const int e = zyfa::launch_fwd(dtype, d_qk, p, maps, grid, reinterpret_cast<cudaStream_t>(stream));
+  const int e = zyfa::launch_fwd(dtype, d_qk, p, maps, grid, device,
+                                 reinterpret_cast<cudaStream_t>(stream));
   return e == 0 ? ZYFA_OK : ZYFA_ERR_LAUNCH;
 }
 

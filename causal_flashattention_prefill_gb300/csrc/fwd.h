@@ -27,9 +27,10 @@ struct TensorMaps {
   CUtensorMap q, k, v;
 };
 
-// Launches the forward kernel for (dtype, d_qk).  Returns a cudaError_t.
+// Launches the forward kernel for (dtype, d_qk) on the current device, whose
+// index (below 64) is `device`.  Returns a cudaError_t.
 int launch_fwd(int dtype, int d_qk, const FwdParams& p, const TensorMaps& maps, int grid,
-               cudaStream_t stream);
+               int device, cudaStream_t stream);
 
 // Dynamic shared memory bytes and swizzle geometry of an instantiation, so the
 // host builds tensor maps whose boxes match the kernel's shared-memory tiles.

@@ -34,6 +34,8 @@
 // end of the sequence read TMA's zero fill; the causal mask already hides
 // such keys from every real query, which is the exact equivalent of padding
 // the sequence with zeros (ZYFA README, "Usage").
+#include <atomic>
+
 #include <cuda_bf16.h>
 
 #include "fwd.h"
@@ -1072,23 +1074,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------- host side
 
+// The dynamic shared-memory limit is raised once per device and
+// instantiation.  Should a launch still be refused (the attribute is lost
+// when a device is reset), it is raised again and the launch retried once.
 template <int DT, int DQK>
-static int launch_one(const FwdParams& p, const TensorMaps& m, int grid, cudaStream_t stream) {
+static int launch_one(const FwdParams& p, const TensorMaps& m, int grid, int device,
+                      cudaStream_t stream) {
   using C = Cfg<DT, DQK>;
+  static std::atomic<uint64_t> attr_set{0};   // bit d: raised on device d
   auto kern = zyfa_fwd_kernel<DT, DQK>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
-  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << device;
+  auto raise_limit = [&]() -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e == cudaSuccess) attr_set.fetch_or(bit, std::memory_order_relaxed);
+    return e;
+  };
+  if (!(attr_set.load(std::memory_order_relaxed) & bit)) {
+    const cudaError_t e = raise_limit();
+    if (e != cudaSuccess) return e;
+  }
   kern<<<grid, kThreads, C::kSmemBytes, stream>>>(m.q, m.k, m.v, p);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaErrorInvalidValue || e == cudaErrorLaunchOutOfResources) {
+    if ((e = raise_limit()) != cudaSuccess) return e;
+    kern<<<grid, kThreads, C::kSmemBytes, stream>>>(m.q, m.k, m.v, p);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 int launch_fwd(int dtype, int d_qk, const FwdParams& p, const TensorMaps& maps, int grid,
-               cudaStream_t stream) {
-  if (dtype == 0 && d_qk == 128) return launch_one<0, 128>(p, maps, grid, stream);
-  if (dtype == 0 && d_qk == 192) return launch_one<0, 192>(p, maps, grid, stream);
-  if (dtype == 1 && d_qk == 128) return launch_one<1, 128>(p, maps, grid, stream);
-  if (dtype == 1 && d_qk == 192) return launch_one<1, 192>(p, maps, grid, stream);
+               int device, cudaStream_t stream) {
+  if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  if (dtype == 0 && d_qk == 128) return launch_one<0, 128>(p, maps, grid, device, stream);
+  if (dtype == 0 && d_qk == 192) return launch_one<0, 192>(p, maps, grid, device, stream);
+  if (dtype == 1 && d_qk == 128) return launch_one<1, 128>(p, maps, grid, device, stream);
+  if (dtype == 1 && d_qk == 192) return launch_one<1, 192>(p, maps, grid, device, stream);
   return cudaErrorInvalidValue;
 }
 
