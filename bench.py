@@ -132,18 +132,106 @@ class ClockSampler:
         os.unlink(self.path)
         if not rows:
             return None
-        loaded = [r for r in rows if r["power"] > 300.0] or rows
+        loaded = [r for r in rows if r["power"] > 300.0]
+        note = None
+        if not loaded:
+            note = ("no nvidia-smi sample fell under load (the timed region is shorter "
+                    "than the 100 ms sampling interval); figures are of all samples")
+            loaded = rows
         reasons = set()
         for r in loaded:
             for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
                               ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
                 if r[key].lower() == "active":
                     reasons.add(name)
-        return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
-                "sm_max_mhz": max(r["max"] for r in rows),
-                "power_w_max": max(r["power"] for r in rows),
-                "samples": len(rows), "samples_under_load": len(loaded),
-                "reasons": sorted(reasons)}
+        out = {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+               "sm_max_mhz": max(r["max"] for r in rows),
+               "power_w_max": max(r["power"] for r in rows),
+               "samples": len(rows), "samples_under_load": 0 if note else len(loaded),
+               "reasons": sorted(reasons), "source": "nvidia-smi -lms 100"}
+        if note:
+            out["note"] = note
+        return out
+
+
+class NvmlClockSampler:
+    """SM clock, power and clock-event reasons read through NVML (ctypes on the
+    driver's libnvidia-ml) every ~2 ms on a background thread, from just
+    before to just after the timed region, so that a region of a few tens of
+    milliseconds still holds samples taken while the kernels run."""
+
+    # nvmlClocksEventReasons bits (nvml.h)
+    REASONS = ((0x4, "sw_power_cap"), (0x8, "hw_slowdown"), (0x20, "sw_thermal_slowdown"),
+               (0x40, "hw_thermal_slowdown"), (0x80, "hw_power_brake_slowdown"))
+
+    def __init__(self, device):
+        import ctypes
+        self.c = ctypes
+        self.ok = False
+        self.samples = []
+        self.stop = False
+        try:
+            import torch
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            p = torch.cuda.get_device_properties(device)
+            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0".encode()
+            self.h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(self.h)) != 0:
+                return
+            self.reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) != 0:   # NVML_CLOCK_SM
+                return
+            self.max_mhz = mx.value
+            self.nv = nv
+            self.ok = True
+        except (OSError, AttributeError, RuntimeError):
+            self.ok = False
+
+    def _read(self):
+        c = self.c
+        mhz, pw, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz))
+        self.nv.nvmlDeviceGetPowerUsage(self.h, c.byref(pw))
+        self.reasons_fn(self.h, c.byref(rs))
+        return time.perf_counter(), mhz.value, pw.value / 1000.0, rs.value
+
+    def _loop(self):
+        while not self.stop:
+            self.samples.append(self._read())
+            time.sleep(0.002)
+
+    def __enter__(self):
+        import threading
+        if self.ok:
+            self.samples.append(self._read())
+            self.th = threading.Thread(target=self._loop, daemon=True)
+            self.th.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self.stop = True
+            self.th.join(timeout=2)
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        reasons = set()
+        for _, _, _, r in self.samples:
+            for bit, name in self.REASONS:
+                if r & bit:
+                    reasons.add(name)
+        sm = [m for _, m, _, _ in self.samples]
+        return {"sm_mhz": statistics.median(sm), "sm_mhz_min": min(sm), "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(p for _, _, p, _ in self.samples),
+                "samples": len(self.samples), "samples_under_load": len(self.samples),
+                "reasons": sorted(reasons),
+                "source": "NVML every ~2 ms during the timed region (power is NVML's "
+                          "running average)"}
 
 
 # -------------------------------------------------------------- GPU timing
@@ -548,7 +636,10 @@ def main():
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     gpu_index = int(visible[device.index]) if len(visible) > device.index and \
         visible[device.index].strip().isdigit() else device.index
-    with ClockSampler(gpu_index) as clk:
+    clk = NvmlClockSampler(device)
+    if not clk.ok:
+        clk = ClockSampler(gpu_index)
+    with clk:
         ms, wall = run_timed(launch, flush, starts, ends, device)
     if world > 1:
         dist.barrier()
