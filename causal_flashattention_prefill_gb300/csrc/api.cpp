@@ -23,6 +23,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 std::atomic<int> g_serialize_pv{0};
+std::atomic<int> g_rounded_p{0};
 
 constexpr int kMaxDevices = 64;
 
@@ -254,6 +255,7 @@ int zyfa_fwd_scaled(const void* q, const void* k, const void* v, void* out, floa
   p.n_qblocks = (S + 255) / 256;
   p.total_items = B * H * p.n_qblocks;
   p.serialize_pv = g_serialize_pv.load(std::memory_order_relaxed);
+  p.rounded_p = g_rounded_p.load(std::memory_order_relaxed);
   p.softmax_scale = softmax_scale;
   const int grid = p.total_items < sms ? p.total_items : sms;
   const int e = zyfa::launch_fwd(dtype, d_qk, p, maps, grid, device,
@@ -297,6 +299,11 @@ int zyfa_device_status(int* value, int reset) {
 int zyfa_set_option(int option, int value) {
   if (option == ZYFA_OPT_SERIALIZE_PV) {
     g_serialize_pv.store(value ? 1 : 0);
+    return ZYFA_OK;
+  }
+  if (option == ZYFA_OPT_ROUNDED_P) {
+    if (value < 0 || value > 2) return ZYFA_ERR_ARG;
+    g_rounded_p.store(value);
     return ZYFA_OK;
   }
   return ZYFA_ERR_ARG;

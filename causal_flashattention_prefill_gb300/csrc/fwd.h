@@ -20,6 +20,8 @@ struct FwdParams {
   int n_qblocks;             // ceil(S / 256): query blocks of two 128-row tiles
   int total_items;           // B * H * n_qblocks
   int serialize_pv;          // verification mode: P fully read before S reuses it
+  int rounded_p;             // 0: default; 1: O's denominator from the rounded P on
+                             // every tile; 2: that and the LSE from the same sum
   float softmax_scale;
 };
 

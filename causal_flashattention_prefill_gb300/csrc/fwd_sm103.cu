@@ -67,9 +67,16 @@ constexpr float exp2i(int n) {
   return r;
 }
 
-template <int DT, int DQK>
+template <int DT, int DQK, int RP = 0>
 struct Cfg {
   static constexpr bool kF8 = DT == 1;
+  // RP: the denominator of O is, on every tile, the sum of the rounded P
+  // values that multiply V (BF16 values; FP8 e4m3 codes, plus the lo term
+  // where the tile has one), so each output row is a weighted average whose
+  // weights sum to one (ZYFA README, "Accuracy").  Without RP that sum is
+  // taken only where one probability carries a large share of the row's
+  // mass, and the unrounded sum stands in elsewhere.
+  static constexpr bool kRoundedP = RP != 0;
   static constexpr int kElem = kF8 ? 1 : 2;
   // Q and K: rows of DQK elements, stored as column chunks of one swizzle
   // span each (128 bytes, or 64 bytes when the row is not a multiple of 128).
@@ -286,6 +293,14 @@ __device__ __forceinline__ float row_max128(const float* f) {
   return fmaxf(row_max64(f), row_max64(f + 64));
 }
 
+// Sum of the four e4m3 values packed in w (exact FP16 values, added in
+// FP32 in byte order).
+__device__ __forceinline__ float e4m3x4_sum(uint32_t w) {
+  float d[4];
+  ptx::unpack_e4m3x4(w, d);
+  return (d[0] + d[1]) + (d[2] + d[3]);
+}
+
 // P for 64 scores (half h of the row): p = 2^(s*c + neg_m) by paired FMAs
 // and exp2, packed to BF16 (or e4m3; with two_term also the e4m3 rounding
 // residual at column offset 32), stored to tensor memory over S.  `sacc`
@@ -322,6 +337,12 @@ __device__ __forceinline__ void produce_half(const float* f, float c_log2, float
 #pragma unroll
         for (int i = 0; i < 8; ++i) *tacc |= pk[i] + tk;
       }
+      if constexpr (C::kRoundedP) {
+        float a2[2] = {0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a2[i & 1] += e4m3x4_sum(pk[i]);
+        rr += a2[0] + a2[1];
+      }
       if (two_term) {
         uint32_t lo[8];
 #pragma unroll
@@ -332,13 +353,19 @@ __device__ __forceinline__ void produce_half(const float* f, float c_log2, float
                                    e[4 * i + 3] - d[3]);
         }
         ptx::tmem_st8(t_s + 32 + ch * 8, lo);
+        if constexpr (C::kRoundedP) {
+          float a2[2] = {0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) a2[i & 1] += e4m3x4_sum(lo[i]);
+          rr += a2[0] + a2[1];
+        }
       }
     } else {
       uint32_t pk[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(e[2 * i], e[2 * i + 1]);
       ptx::tmem_st16(t_s + ch * 16, pk);
-      if constexpr (kExact) {
+      if constexpr (kExact || C::kRoundedP) {
         float a2[2] = {0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 16; ++i) a2[i & 1] = ptx::add_bf16x2_f32(a2[i & 1], pk[i]);
@@ -361,12 +388,16 @@ __device__ __forceinline__ uint32_t threshold_addend(uint32_t c) {
 // unrounded sum rs, from one exp2 pass (hi and rs are the values, in the
 // same order, that produce_tile gives).  Without do_hi the hi codes in
 // tensor memory are those this pass would store.
+//   With kRoundedP the sum of the rounded values that multiply V is also
+// formed: rr becomes the sum of hi and lo with do_hi, and gains the sum of
+// lo without (the hi codes then being those already summed).
 template <class C>
 __device__ __forceinline__ void redo_fp8(const float* f, float c_log2, float neg_m,
-                                         uint32_t t_s, bool do_hi, float& rs) {
+                                         uint32_t t_s, bool do_hi, float& rs, float& rr) {
   const float2 c2 = make_float2(c_log2, c_log2);
   const float2 nm2 = make_float2(neg_m, neg_m);
   float2 sacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+  float ra[2] = {0.f, 0.f};
 #pragma unroll
   for (int ch = 0; ch < 4; ++ch) {
     uint32_t hi[8], lo[8];
@@ -389,11 +420,19 @@ __device__ __forceinline__ void redo_fp8(const float* f, float c_log2, float neg
     }
     if (do_hi) ptx::tmem_st8(t_s + ch * 8, hi);
     ptx::tmem_st8(t_s + 32 + ch * 8, lo);
+    if constexpr (C::kRoundedP) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (do_hi) ra[i & 1] += e4m3x4_sum(hi[i]);
+        ra[i & 1] += e4m3x4_sum(lo[i]);
+      }
+    }
   }
   if (do_hi) {
     const float2 t2 = __fadd2_rn(sacc[0], sacc[1]);
     rs = t2.x + t2.y;
   }
+  if constexpr (C::kRoundedP) rr = (do_hi ? 0.f : rr) + (ra[0] + ra[1]);
 }
 
 // BF16: the sum rr of the rounded P of the row (the values that multiply
@@ -444,12 +483,12 @@ __device__ __forceinline__ void produce_tile(const float* f, float c_log2, float
 
 }  // namespace
 
-template <int DT, int DQK>
+template <int DT, int DQK, int RP>
 __global__ void __launch_bounds__(kThreads, 1)
     zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = Cfg<DT, DQK>;
+  using C = Cfg<DT, DQK, RP>;
   constexpr int NS = C::kNumPieces;
   using B = Bars<NS>;
 
@@ -1000,7 +1039,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (right after a rescale its maximum carries most of the mass
             // the row has seen, so the test below would pass anyway).
             two_term = any_need || diag || __any_sync(0xffffffffu, p_max * 32.0f > l + rs);
-            if (two_term) redo_fp8<C>(f, c_log2, neg_m, t_s, any_need, rs);
+            if (two_term) redo_fp8<C>(f, c_log2, neg_m, t_s, any_need, rs, rr);
           } else {
             // A recomputed tile takes the rounded-sum denominator in the same
             // exp2 pass (right after a rescale its maximum carries most of
@@ -1020,7 +1059,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         l += rs;
-        lr += exact ? rr : rs;
+        lr += (exact || C::kRoundedP) ? rr : rs;
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
@@ -1061,8 +1100,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (valid && p.lse != nullptr) {
+        // Mode 2 takes the LSE from the same rounded sum as the
+        // denominator (results over different key ranges then merge
+        // consistently; ZYFA README, "Accuracy").
+        const float lsum = (C::kRoundedP && p.rounded_p == 2) ? lr : l;
         p.lse[(static_cast<int64_t>(it.b) * p.H + it.h) * p.S + row] =
-            (m_ref + log2f(l) - C::kPLog2Scale) * 0.6931471805599453f;
+            (m_ref + log2f(lsum) - C::kPLog2Scale) * 0.6931471805599453f;
       }
       ptx::tc_fence_before();
     }
@@ -1080,12 +1123,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The dynamic shared-memory limit is raised once per device and
 // instantiation.  Should a launch still be refused (the attribute is lost
 // when a device is reset), it is raised again and the launch retried once.
-template <int DT, int DQK>
+template <int DT, int DQK, int RP>
 static int launch_one(const FwdParams& p, const TensorMaps& m, int grid, int device,
                       cudaStream_t stream) {
-  using C = Cfg<DT, DQK>;
+  using C = Cfg<DT, DQK, RP>;
   static std::atomic<uint64_t> attr_set{0};   // bit d: raised on device d
-  auto kern = zyfa_fwd_kernel<DT, DQK>;
+  auto kern = zyfa_fwd_kernel<DT, DQK, RP>;
   const uint64_t bit = 1ull << device;
   auto raise_limit = [&]() -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1110,10 +1153,17 @@ static int launch_one(const FwdParams& p, const TensorMaps& m, int grid, int dev
 int launch_fwd(int dtype, int d_qk, const FwdParams& p, const TensorMaps& maps, int grid,
                int device, cudaStream_t stream) {
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-  if (dtype == 0 && d_qk == 128) return launch_one<0, 128>(p, maps, grid, device, stream);
-  if (dtype == 0 && d_qk == 192) return launch_one<0, 192>(p, maps, grid, device, stream);
-  if (dtype == 1 && d_qk == 128) return launch_one<1, 128>(p, maps, grid, device, stream);
-  if (dtype == 1 && d_qk == 192) return launch_one<1, 192>(p, maps, grid, device, stream);
+  if (p.rounded_p == 0) {
+    if (dtype == 0 && d_qk == 128) return launch_one<0, 128, 0>(p, maps, grid, device, stream);
+    if (dtype == 0 && d_qk == 192) return launch_one<0, 192, 0>(p, maps, grid, device, stream);
+    if (dtype == 1 && d_qk == 128) return launch_one<1, 128, 0>(p, maps, grid, device, stream);
+    if (dtype == 1 && d_qk == 192) return launch_one<1, 192, 0>(p, maps, grid, device, stream);
+  } else {
+    if (dtype == 0 && d_qk == 128) return launch_one<0, 128, 1>(p, maps, grid, device, stream);
+    if (dtype == 0 && d_qk == 192) return launch_one<0, 192, 1>(p, maps, grid, device, stream);
+    if (dtype == 1 && d_qk == 128) return launch_one<1, 128, 1>(p, maps, grid, device, stream);
+    if (dtype == 1 && d_qk == 192) return launch_one<1, 192, 1>(p, maps, grid, device, stream);
+  }
   return cudaErrorInvalidValue;
 }
 

@@ -135,9 +135,23 @@ ZYFA_API int zyfa_device_status(int* value, int reset);
  *   finish before the next score product of the same query tile overwrites
  *   the tensor memory that holds P.  Results are identical; it exists to
  *   verify that the default pipelined order is race-free.  Default 0.
+ *   ZYFA_OPT_ROUNDED_P: how the sums of the probabilities are formed (the
+ *   ZYFA README, "Accuracy" and "Kernel design": the output is divided by
+ *   the sum of the same rounded probabilities that multiply V, and the FP8
+ *   log-sum-exp comes from the rounded probabilities so that results over
+ *   different key ranges merge consistently).
+ *     0 (default): the denominator is the sum of the rounded P (the BF16
+ *       values, or for FP8 the two e4m3 terms) on tiles where one
+ *       probability carries a large share of the row's mass, the unrounded
+ *       sum elsewhere; the LSE comes from the unrounded sum.
+ *     1: the denominator is the sum of the rounded P that multiplies V on
+ *       every tile, so each output row is a weighted average whose weights
+ *       sum to one; the LSE as in 0.
+ *     2: as 1, and the LSE is taken from that same rounded sum.
+ *   Modes 1 and 2 add work to every tile of the softmax (slower).
  * Returns ZYFA_OK or ZYFA_ERR_ARG.
  */
-enum { ZYFA_OPT_SERIALIZE_PV = 1 };
+enum { ZYFA_OPT_SERIALIZE_PV = 1, ZYFA_OPT_ROUNDED_P = 2 };
 ZYFA_API int zyfa_set_option(int option, int value);
 
 /*

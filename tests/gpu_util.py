@@ -130,9 +130,9 @@ def elementwise_bound(Oref: np.ndarray, tol: float) -> np.ndarray:
     return np.where(0.5 * ulp >= tol, ulp, tol)
 
 
-def assert_parity(O, L, Oref, Lref, dtype: str, label: str = ""):
+def assert_parity(O, L, Oref, Lref, dtype: str, label: str = "", tol: Tol = None):
     e = errors(O, L, Oref, Lref)
-    tol = TOL[dtype]
+    tol = TOL[dtype] if tol is None else tol
     bound = elementwise_bound(Oref, tol.max_o)
     dO = np.abs(O - Oref)
     e["n_faithful_only"] = int(np.sum((dO > tol.max_o) & (dO <= bound)))

@@ -41,7 +41,8 @@ def test_header_enums_match_binding():
     text = open(os.path.join(ROOT, "include", "zyfa.h")).read()
     for name in ("ZYFA_OK", "ZYFA_ERR_ARG", "ZYFA_ERR_UNSUPPORTED", "ZYFA_ERR_ALIGN",
                  "ZYFA_ERR_LAUNCH", "ZYFA_ERR_DEVICE", "ZYFA_ERR_DEVICE_TIMEOUT", "ZYFA_BF16",
-                 "ZYFA_FP8_E4M3", "ZYFA_BSHD", "ZYFA_BHSD", "ZYFA_OPT_SERIALIZE_PV"):
+                 "ZYFA_FP8_E4M3", "ZYFA_BSHD", "ZYFA_BHSD", "ZYFA_OPT_SERIALIZE_PV",
+                 "ZYFA_OPT_ROUNDED_P"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m, name
         assert int(m.group(1)) == getattr(zf, name), name
@@ -126,6 +127,10 @@ def test_fwd_rejects_before_any_cuda_call(lib, kw, expected):
 def test_options(lib):
     assert zf.zyfa_set_option(zf.ZYFA_OPT_SERIALIZE_PV, 1) == zf.ZYFA_OK
     assert zf.zyfa_set_option(zf.ZYFA_OPT_SERIALIZE_PV, 0) == zf.ZYFA_OK
+    for mode in (1, 2, 0):
+        assert zf.zyfa_set_option(zf.ZYFA_OPT_ROUNDED_P, mode) == zf.ZYFA_OK
+    assert zf.zyfa_set_option(zf.ZYFA_OPT_ROUNDED_P, 3) == zf.ZYFA_ERR_ARG
+    assert zf.zyfa_set_option(zf.ZYFA_OPT_ROUNDED_P, -1) == zf.ZYFA_ERR_ARG
     assert zf.zyfa_set_option(99, 1) == zf.ZYFA_ERR_ARG
 
 
