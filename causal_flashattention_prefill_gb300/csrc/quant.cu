@@ -184,6 +184,11 @@ constexpr int kRotTileRows = 64;
 constexpr int kRotConsumers = 4;                       // warps that rotate
 constexpr int kRotThreads = 32 * (kRotConsumers + 1);  // + one producer warp
 constexpr int kRotSmemTarget = 64 * 1024;              // ring bytes per CTA (at least two stages)
+// L2 reuse between the passes: the first pass reads the last tiles of x
+// (those it loads last, up to this many bytes) with an evict_last hint and
+// the others with evict_first, and the second pass walks every CTA's tiles
+// in reverse order, so its first reads find them in L2.
+constexpr int64_t kRotL2KeepBytes = int64_t(88) << 20;
 
 // Status word of these kernels (bit 0: a wait timed out).
 __device__ int g_rot_status;
@@ -324,6 +329,64 @@ __device__ __forceinline__ void rot_half(float (&v)[D / 2], const float* s_signs
   }
 }
 
+// BF16 input: this lane's half of row r rotated as rot_half does, with the
+// butterfly stride that pairs the two lanes of the row taken first, on the
+// raw BF16 words (Hadamard stages commute; only the FP32 rounding order
+// differs).  The signs come as XOR masks (bit 15 / 31 flips the BF16 value
+// in the low / high half of a word), so a shuffle of one 32-bit word moves
+// two values across the lane pair.
+template <int D>
+__device__ __forceinline__ void rot_half_bf16(const uint8_t* tile, int r, int p,
+                                              const uint32_t (&mask)[D / 4], float (&v)[D / 2]) {
+  using T = RotTile<D, kQuantBF16>;
+  const float sgn = p ? -1.0f : 1.0f;
+  const float2 s2 = make_float2(sgn, sgn);
+#pragma unroll
+  for (int k = 0; k < T::kChunks; ++k) {
+    const int byte = RotHalf<D>::channel(k * T::kPerChunk, p) * 2;
+    const int box = byte >> 7, c16 = (byte & 127) >> 4;
+    const uint4 w4 = *reinterpret_cast<const uint4*>(tile + box * T::kBoxBytes + r * 128 +
+                                                     ((c16 ^ (r & 7)) << 4));
+    const uint32_t u[4] = {w4.x ^ mask[4 * k], w4.y ^ mask[4 * k + 1], w4.z ^ mask[4 * k + 2],
+                           w4.w ^ mask[4 * k + 3]};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t o = __shfl_xor_sync(0xffffffffu, u[q], 16);
+      // lower lane: own + partner; upper lane: partner - own
+      const float2 mine = make_float2(__uint_as_float(u[q] << 16), __uint_as_float(u[q] & 0xFFFF0000u));
+      const float2 other = make_float2(__uint_as_float(o << 16), __uint_as_float(o & 0xFFFF0000u));
+      const float2 y = __ffma2_rn(mine, s2, other);
+      v[8 * k + 2 * q] = y.x;
+      v[8 * k + 2 * q + 1] = y.y;
+    }
+  }
+  if constexpr (D == 128) {
+    fwht_local<64>(v, 0);
+  } else {
+#pragma unroll
+    for (int a = 0; a < 3; ++a) fwht_local<32>(v, 32 * a);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const float b0 = v[e], b1 = v[32 + e], b2 = v[64 + e];
+      v[e] = (b0 + b1) + b2;
+      v[32 + e] = b0 - b2;
+      v[64 + e] = (b0 - 2.0f * b1) + b2;
+    }
+  }
+}
+
+// XOR masks of the signs for this lane's half (see rot_half_bf16): word j
+// covers local values 2j and 2j + 1.
+template <int D>
+__device__ __forceinline__ void rot_sign_masks(const float* s_signs, int p,
+                                               uint32_t (&mask)[D / 4]) {
+  constexpr int kN = D / 2;
+  const float* sg = s_signs + p * (kN + 1);
+#pragma unroll
+  for (int j = 0; j < D / 4; ++j)
+    mask[j] = (sg[2 * j] < 0.f ? 0x8000u : 0u) | (sg[2 * j + 1] < 0.f ? 0x80000000u : 0u);
+}
+
 // Codes are staged in shared memory, eight rows of a warp at a time (16-byte
 // chunk c of row r at chunk rot_code_chunk(c, r) of that row), so that each
 // global store writes 512 contiguous bytes.  The permutation keeps both the
@@ -377,7 +440,8 @@ __device__ __forceinline__ bool rot_warp_wait(uint32_t b, uint32_t parity, volat
 // One pass over the tensor.  kQuant = false: each CTA writes max |x @ R| of
 // its tiles to partial[blockIdx.x].  kQuant = true: every CTA reduces the
 // num_partials maxima to the descale, CTA 0 stores it, and each row's codes
-// are written to x8.  Tiles t = blockIdx.x + i * gridDim.x.
+// are written to x8.  CTA b takes tiles b + i * gridDim.x, i ascending in
+// the first pass and descending in the second.
 template <int D, int XT, bool kQuant>
 __global__ void __launch_bounds__(kRotThreads)
     rot_pass_kernel(const __grid_constant__ CUtensorMap tm, int64_t rows, const float* signs,
@@ -428,18 +492,26 @@ __global__ void __launch_bounds__(kRotThreads)
     __syncthreads();
   }
   const int64_t n_tiles = (rows + kRotTileRows - 1) / kRotTileRows;
+  const int64_t n_mine =
+      n_tiles > blockIdx.x ? (n_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  // k-th tile of this CTA (k counts ring uses in both roles).
+  auto tile_of = [&](int64_t k) {
+    return static_cast<int64_t>(blockIdx.x) + (kQuant ? n_mine - 1 - k : k) * gridDim.x;
+  };
 
   if (warp == kRotConsumers) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       ptx::prefetch_tmap(&tm);
-      // The first pass leaves x in L2 for the second where it fits; the
-      // second reads it for the last time.
-      const uint64_t pol = kQuant ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+      // The first pass leaves its last tiles of x in L2 for the second; the
+      // second reads x for the last time.
+      const uint64_t pol_first = ptx::policy_evict_first();
+      const uint64_t pol_last = ptx::policy_evict_last();
+      const int64_t keep_from = n_tiles - kRotL2KeepBytes / T::kTileBytes;
       uint32_t armed = 0, par = 0;  // bit st: armed at least once / parity of its last arming
-      for (int64_t i = 0;; ++i) {
-        const int64_t tile = blockIdx.x + i * gridDim.x;
-        if (tile >= n_tiles) break;
+      for (int64_t i = 0; i < n_mine; ++i) {
+        const int64_t tile = tile_of(i);
+        const uint64_t pol = (!kQuant && tile >= keep_from) ? pol_last : pol_first;
         const int st = static_cast<int>(i % NS);
         const uint32_t round = static_cast<uint32_t>(i / NS);
         if (!ptx::mbar_wait(empty(st), (round & 1u) ^ 1u, abort, &g_rot_status, 1)) break;
@@ -461,14 +533,22 @@ __global__ void __launch_bounds__(kRotThreads)
     // ------------------------------------------------------------ rotation
     const int r = 16 * warp + (lane & 15);  // row within the tile
     const int p = lane >> 4;                // half of the row
+    // BF16 at d = 128 takes the sign-mask path (rot_half_bf16); at d = 192
+    // its 48 mask registers would cost a CTA per SM (measured slower).
+    constexpr bool kMaskPath = XT == kQuantBF16 && D == 128;
+    uint32_t mask[kMaskPath ? D / 4 : 1];
+    if constexpr (kMaskPath) rot_sign_masks<D>(s_signs, p, mask);
     float m = 0.f;
-    for (int64_t i = 0;; ++i) {
-      const int64_t tile = blockIdx.x + i * gridDim.x;
-      if (tile >= n_tiles) break;
+    for (int64_t i = 0; i < n_mine; ++i) {
+      const int64_t tile = tile_of(i);
       const int st = static_cast<int>(i % NS);
       if (!rot_warp_wait(full(st), static_cast<uint32_t>(i / NS) & 1u, abort, lane)) break;
       float v[D / 2];
-      rot_read_half<D, XT>(ring + st * T::kTileBytes, r, p, v);
+      if constexpr (kMaskPath) {
+        rot_half_bf16<D>(ring + st * T::kTileBytes, r, p, mask, v);
+      } else {
+        rot_read_half<D, XT>(ring + st * T::kTileBytes, r, p, v);
+      }
       // The stage goes back to the tensor copies (async proxy) after these
       // generic-proxy reads: order them before the release.
       ptx::fence_proxy_async_smem();
@@ -476,7 +556,7 @@ __global__ void __launch_bounds__(kRotThreads)
       if (lane == 0) ptx::mbar_arrive(empty(st));
       // Rows past the end read TMA's zero fill: they rotate to zero and
       // leave the maximum unchanged; their codes are not stored.
-      rot_half<D>(v, s_signs, p);
+      if constexpr (!kMaskPath) rot_half<D>(v, s_signs, p);
       if constexpr (!kQuant) {
 #pragma unroll
         for (int a = 0; a < D / 64; ++a) {
