@@ -24,6 +24,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 
 std::atomic<int> g_serialize_pv{0};
 std::atomic<int> g_rounded_p{0};
+std::atomic<int> g_block_scale{0};
 
 constexpr int kMaxDevices = 64;
 
@@ -256,6 +257,7 @@ int zyfa_fwd_scaled(const void* q, const void* k, const void* v, void* out, floa
   p.total_items = B * H * p.n_qblocks;
   p.serialize_pv = g_serialize_pv.load(std::memory_order_relaxed);
   p.rounded_p = g_rounded_p.load(std::memory_order_relaxed);
+  p.block_scale = g_block_scale.load(std::memory_order_relaxed);
   p.softmax_scale = softmax_scale;
   const int grid = p.total_items < sms ? p.total_items : sms;
   const int e = zyfa::launch_fwd(dtype, d_qk, p, maps, grid, device,
@@ -304,6 +306,11 @@ int zyfa_set_option(int option, int value) {
   if (option == ZYFA_OPT_ROUNDED_P) {
     if (value < 0 || value > 2) return ZYFA_ERR_ARG;
     g_rounded_p.store(value);
+    return ZYFA_OK;
+  }
+  if (option == ZYFA_OPT_BLOCK_SCALE) {
+    if (value < 0 || value > 1) return ZYFA_ERR_ARG;
+    g_block_scale.store(value);
     return ZYFA_OK;
   }
   return ZYFA_ERR_ARG;

@@ -22,6 +22,7 @@ struct FwdParams {
   int serialize_pv;          // verification mode: P fully read before S reuses it
   int rounded_p;             // 0: default; 1: O's denominator from the rounded P on
                              // every tile; 2: that and the LSE from the same sum
+  int block_scale;           // FP8: P scaled per 32-key slice, block-scaled P V
   float softmax_scale;
 };
 

@@ -67,9 +67,18 @@ constexpr float exp2i(int n) {
   return r;
 }
 
-template <int DT, int DQK, int RP = 0>
+template <int DT, int DQK, int RP = 0, int BS = 0>
 struct Cfg {
   static constexpr bool kF8 = DT == 1;
+  // BS (FP8): per-block scaling of P (ZYFA README, "Kernel design",
+  // per-block scaling).  Each row's P is scaled per 32-key slice by the
+  // power of two that brings the slice's largest value to the binade of
+  // p = 1, so that small probabilities stay normal e4m3 values, and the P V
+  // product is the block-scaled MMA (kind::mxf8f6f4), which multiplies each
+  // slice by the inverse power of two (a UE8M0 scale factor per row and
+  // slice) as it accumulates.
+  static constexpr bool kBlockScale = BS != 0;
+  static_assert(!kBlockScale || kF8, "block scaling is an FP8 form");
   // RP: the denominator of O is, on every tile, the sum of the rounded P
   // values that multiply V (BF16 values; FP8 e4m3 codes, plus the lo term
   // where the tile has one), so each output row is a weighted average whose
@@ -118,7 +127,9 @@ struct Cfg {
   // from moving after the first tiles, so exp2 can run against it before
   // the tile maximum is known: BF16 16 (p <= 2^16, far inside BF16 and the
   // FP32 sums and accumulators), FP8 4 (p * 2^4 <= 256, inside e4m3's 448).
-  static constexpr int kTauBits = kF8 ? 4 : 16;
+  // With block scaling, P never exceeds 32 (each slice is normalised), so
+  // FP8 takes the BF16 threshold.
+  static constexpr int kTauBits = (kF8 && !kBlockScale) ? 4 : 16;
   static constexpr float kTau = static_cast<float>(kTauBits);
   // FP8 P is stored as e4m3 of p * 2^4 (p <= 2^tau keeps it below 448); the
   // factor enters as +4 in the exponent.
@@ -132,6 +143,11 @@ struct Cfg {
   static constexpr uint32_t kFmt = kF8 ? 0u : 1u;   // E4M3 / BF16
   static constexpr uint32_t kIdescQK = ptx::instr_desc(kFmt, kFmt, 0, kBM, kBN);
   static constexpr uint32_t kIdescPV = ptx::instr_desc(kFmt, kFmt, 1, kBM, kDV);
+  // Block-scaled P V, K slice ks (one MMA): byte ks of the scale-factor words.
+  __host__ __device__ static constexpr uint32_t idesc_pv_bs(int ks) {
+    return ptx::instr_desc_bs(0u, 0u, 1u, kBM, kDV, static_cast<uint32_t>(ks),
+                              static_cast<uint32_t>(ks));
+  }
   // Register split: the MMA issuer of the d_qk = 192 BF16 form unrolls 12
   // K steps and needs more registers than the others.
   static constexpr int kSoftmaxRegs = (!kF8 && DQK == 192) ? 184 : 200;
@@ -291,6 +307,51 @@ __device__ __forceinline__ float row_max64(const float* f) {
 
 __device__ __forceinline__ float row_max128(const float* f) {
   return fmaxf(row_max64(f), row_max64(f + 64));
+}
+
+// Maximum of 32 scores (two chains of three-input max).
+__device__ __forceinline__ float row_max32(const float* f) {
+  float a = ptx::max3(f[0], f[1], f[2]);
+  float b = ptx::max3(f[3], f[4], f[5]);
+#pragma unroll
+  for (int k = 6; k < 30; k += 4) {
+    a = ptx::max3(a, f[k], f[k + 1]);
+    b = ptx::max3(b, f[k + 2], f[k + 3]);
+  }
+  return ptx::max3(a, b, fmaxf(f[30], f[31]));
+}
+
+// Tensor-memory columns of a stage's S region that hold, once the softmax
+// has read S, the scale factors of the block-scaled P V: those of P (one
+// 32-bit word per row, byte k for key slice k; the rows of lane quarter q
+// in column kSfaCol + q) and those of V (all 2^0).
+constexpr uint32_t kSfaCol = 64;
+constexpr uint32_t kSfbCol = 96;
+
+// Exponent e of the power of two 2^e that brings the largest P of a 32-key
+// slice, 2^y with y = (slice maximum) * c - m_ref, into the binade of p = 1:
+// e = -floor(y), kept within [-32, 100] (an entirely masked slice has
+// y = -inf; its P is zero under any scale).
+__device__ __forceinline__ float slice_exponent(float xm, float c_log2, float m_ref) {
+  const float y = fmaf(xm, c_log2, -m_ref);
+  return fminf(fmaxf(-floorf(y), -32.0f), 100.0f);
+}
+
+// 2^-e for an integral e in [-32, 100], exactly.
+__device__ __forceinline__ float pow2_neg(float e) {
+  return __int_as_float((127 - static_cast<int>(e)) << 23);
+}
+
+// O of the row times alpha, in tensor memory.
+__device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha) {
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    uint32_t o[32];
+    ptx::tmem_ld32_wait(t_o + c * 32, o);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+    ptx::tmem_st32(t_o + c * 32, o);
+  }
 }
 
 // Sum of the four e4m3 values packed in w (exact FP16 values, added in
@@ -467,6 +528,65 @@ __device__ __forceinline__ void redo_bf16(const float* f, float c_log2, float ne
   }
 }
 
+// FP8 with per-slice scales: for key slice k of the row, P' = 2^(s*c + neg_m
+// + e_k) (the slice's largest value in [16, 32) when the slice is not
+// clamped), hi codes stored at column 8k and with kLo the e4m3 rounding
+// residual at 32 + 8k.  With kHi, rs = the unrounded sum of P = P' 2^-e_k
+// over the row.  With kRoundedP, rr gains the sum of the rounded values
+// that multiply V (hi with kHi, lo with kLo), each slice times 2^-e_k.
+// Without kHi the pass recomputes hi only to form lo (the hi codes in
+// tensor memory are those it would store).
+template <class C, bool kHi, bool kLo>
+__device__ __forceinline__ void produce_bs(const float* f, float c_log2, float neg_m,
+                                           const float (&ex)[4], uint32_t t_s, float& rs,
+                                           float& rr) {
+  const float2 c2 = make_float2(c_log2, c_log2);
+  float rsum = 0.f;
+#pragma unroll
+  for (int ch = 0; ch < 4; ++ch) {
+    const float bias = neg_m + ex[ch];
+    const float2 b2 = make_float2(bias, bias);
+    const float down = pow2_neg(ex[ch]);
+    float2 sacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 xa =
+          __ffma2_rn(make_float2(f[32 * ch + 4 * i], f[32 * ch + 4 * i + 1]), c2, b2);
+      const float2 xb =
+          __ffma2_rn(make_float2(f[32 * ch + 4 * i + 2], f[32 * ch + 4 * i + 3]), c2, b2);
+      const float e0 = ptx::ex2(xa.x), e1 = ptx::ex2(xa.y), e2 = ptx::ex2(xb.x),
+                  e3 = ptx::ex2(xb.y);
+      if constexpr (kHi) {
+        sacc[0] = __fadd2_rn(sacc[0], make_float2(e0, e1));
+        sacc[1] = __fadd2_rn(sacc[1], make_float2(e2, e3));
+      }
+      hi[i] = ptx::pack_e4m3x4(e0, e1, e2, e3);
+      if constexpr (kLo) {
+        float d[4];
+        ptx::unpack_e4m3x4(hi[i], d);
+        lo[i] = ptx::pack_e4m3x4(e0 - d[0], e1 - d[1], e2 - d[2], e3 - d[3]);
+      }
+    }
+    if constexpr (kHi) ptx::tmem_st8(t_s + ch * 8, hi);
+    if constexpr (kLo) ptx::tmem_st8(t_s + 32 + ch * 8, lo);
+    if constexpr (kHi) {
+      const float2 t2 = __fadd2_rn(sacc[0], sacc[1]);
+      rsum += (t2.x + t2.y) * down;
+    }
+    if constexpr (C::kRoundedP) {
+      float a2[2] = {0.f, 0.f};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if constexpr (kHi) a2[i & 1] += e4m3x4_sum(hi[i]);
+        if constexpr (kLo) a2[i & 1] += e4m3x4_sum(lo[i]);
+      }
+      rr += (a2[0] + a2[1]) * down;
+    }
+  }
+  if constexpr (kHi) rs = rsum;
+}
+
 // P for the whole 128-score row against reference neg_m; rs = unrounded
 // sum, rr = sum of the rounded values (with kRR, BF16).  The variant is a
 // template argument so that each call site carries only the code it runs.
@@ -483,12 +603,12 @@ __device__ __forceinline__ void produce_tile(const float* f, float c_log2, float
 
 }  // namespace
 
-template <int DT, int DQK, int RP>
+template <int DT, int DQK, int RP, int BS>
 __global__ void __launch_bounds__(kThreads, 1)
     zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = Cfg<DT, DQK, RP>;
+  using C = Cfg<DT, DQK, RP, BS>;
   constexpr int NS = C::kNumPieces;
   using B = Bars<NS>;
 
@@ -745,10 +865,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dv = dv0 + (Ring<C>::v_chunk(vb, 0) >> 4);
         const uint32_t a_tmem = tmem + s * 128 + p_col;
         const uint32_t d_tmem = tmem + 256 + s * 128;
+        if constexpr (C::kBlockScale) {
+          // Slice ks of P (keys 32 ks .. 32 ks + 31) with its scale factors.
+          const uint32_t sfa = tmem + s * 128 + kSfaCol, sfb = tmem + s * 128 + kSfbCol;
 #pragma unroll
-        for (int ks = 0; ks < kBN / C::kUmmaK; ++ks)
-          ptx::mma_ts_elect<C::kF8>(d_tmem, a_tmem + ks * 8, dv + ((ks * C::kUmmaK * 128) >> 4),
-                              C::kIdescPV, (acc_first || ks > 0) ? 1u : 0u);
+          for (int ks = 0; ks < kBN / C::kUmmaK; ++ks)
+            ptx::mma_ts_bs_elect(d_tmem, a_tmem + ks * 8, dv + ((ks * C::kUmmaK * 128) >> 4),
+                                 C::idesc_pv_bs(ks), sfa, sfb, (acc_first || ks > 0) ? 1u : 0u);
+        } else {
+#pragma unroll
+          for (int ks = 0; ks < kBN / C::kUmmaK; ++ks)
+            ptx::mma_ts_elect<C::kF8>(d_tmem, a_tmem + ks * 8,
+                                      dv + ((ks * C::kUmmaK * 128) >> 4), C::kIdescPV,
+                                      (acc_first || ks > 0) ? 1u : 0u);
+        }
       };
 
       for (int r = 0; ok; ++r) {
@@ -968,7 +1098,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         // rounding errors average out and the unrounded sum stands in.
         float rs = 0.f, rr = 0.f;
         bool exact = false, two_term = false;
-        if (j == 0) {
+        if constexpr (C::kBlockScale) {
+          // Per-slice scales need each slice's maximum before its exp2, so
+          // the tile maximum is known first and a rescale of O, when the
+          // maximum passes the reference by more than tau, precedes P (no
+          // recomputation).  Two-term P as below: on the first tile, the
+          // diagonal tile, a rescaled tile, and where one probability
+          // carries at least 1/32 of the row's mass.
+          float xm[4];
+          xm[0] = row_max32(f);
+          wait_rest();
+          xm[1] = row_max32(f + 32);
+          xm[2] = row_max32(f + 64);
+          xm[3] = row_max32(f + 96);
+          const float mx = fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3])) * c_log2;
+          bool any_need = false;
+          if (j == 0) {
+            m_ref = mx;
+          } else {
+            const bool need = mx > m_ref + C::kTau;
+            any_need = __any_sync(0xffffffffu, need);
+            if (any_need) {
+              const float alpha = need ? ptx::ex2(m_ref - mx) : 1.0f;
+              if (need) {
+                l *= alpha;
+                lr *= alpha;
+                m_ref = mx;
+              }
+              rescale_o(t_o, alpha);
+            }
+          }
+          const float neg_m = C::kPLog2Scale - m_ref;
+          float ex[4];
+          uint32_t sfw = 0;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            ex[k] = slice_exponent(xm[k], c_log2, m_ref);
+            sfw |= static_cast<uint32_t>(127 - static_cast<int>(ex[k])) << (8 * k);
+          }
+          const uint32_t unit[4] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu};
+          ptx::tmem_st1(t_s + kSfaCol + wq, sfw);
+          ptx::tmem_st4(t_s + kSfbCol, unit);
+          if (j == 0 || diag || any_need) {
+            two_term = true;
+            produce_bs<C, true, true>(f, c_log2, neg_m, ex, t_s, rs, rr);
+          } else {
+            produce_bs<C, true, false>(f, c_log2, neg_m, ex, t_s, rs, rr);
+            const float p_max = ptx::ex2(mx + neg_m);
+            two_term = __any_sync(0xffffffffu, p_max * C::kAccRatio > l + rs);
+            if (two_term) produce_bs<C, false, true>(f, c_log2, neg_m, ex, t_s, rs, rr);
+          }
+        } else if (j == 0) {
           // First tile of the row: the reference is this tile's maximum.
           wait_rest();
           m_ref = row_max128(f) * c_log2;
@@ -1017,15 +1197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               lr *= alpha;
               m_ref = mx;
             }
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              uint32_t o[32];
-              ptx::tmem_ld32_wait(t_o + c * 32, o);
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              ptx::tmem_st32(t_o + c * 32, o);
-            }
+            rescale_o(t_o, alpha);
             // P of this tile is computed again below (redo_*) against the
             // moved reference, exactly the values a non-speculative pass
             // would have produced, once the speculative stores to the same
@@ -1123,12 +1295,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The dynamic shared-memory limit is raised once per device and
 // instantiation.  Should a launch still be refused (the attribute is lost
 // when a device is reset), it is raised again and the launch retried once.
-template <int DT, int DQK, int RP>
+template <int DT, int DQK, int RP, int BS = 0>
 static int launch_one(const FwdParams& p, const TensorMaps& m, int grid, int device,
                       cudaStream_t stream) {
-  using C = Cfg<DT, DQK, RP>;
+  using C = Cfg<DT, DQK, RP, BS>;
   static std::atomic<uint64_t> attr_set{0};   // bit d: raised on device d
-  auto kern = zyfa_fwd_kernel<DT, DQK, RP>;
+  auto kern = zyfa_fwd_kernel<DT, DQK, RP, BS>;
   const uint64_t bit = 1ull << device;
   auto raise_limit = [&]() -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1153,6 +1325,16 @@ static int launch_one(const FwdParams& p, const TensorMaps& m, int grid, int dev
 int launch_fwd(int dtype, int d_qk, const FwdParams& p, const TensorMaps& maps, int grid,
                int device, cudaStream_t stream) {
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  if (dtype == 1 && p.block_scale) {
+    if (p.rounded_p == 0) {
+      if (d_qk == 128) return launch_one<1, 128, 0, 1>(p, maps, grid, device, stream);
+      if (d_qk == 192) return launch_one<1, 192, 0, 1>(p, maps, grid, device, stream);
+    } else {
+      if (d_qk == 128) return launch_one<1, 128, 1, 1>(p, maps, grid, device, stream);
+      if (d_qk == 192) return launch_one<1, 192, 1, 1>(p, maps, grid, device, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (p.rounded_p == 0) {
     if (dtype == 0 && d_qk == 128) return launch_one<0, 128, 0>(p, maps, grid, device, stream);
     if (dtype == 0 && d_qk == 192) return launch_one<0, 192, 0>(p, maps, grid, device, stream);

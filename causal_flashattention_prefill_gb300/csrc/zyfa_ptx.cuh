@@ -217,6 +217,18 @@ __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_fmt, uint32_t b_fmt
          | ((M >> 4) << 24);      // M / 16
 }
 
+// Instruction descriptor of the block-scaled kind (kind::mxf8f6f4): no D
+// format field (D is FP32); bits 4-5 and 29-30 pick the byte of the 32-bit
+// tensor-memory word that holds the scale factor of B and of A for this
+// MMA's 32-deep slice of K; bit 23 = 1 selects UE8M0 scale factors (a power
+// of two 2^(e - 127) per byte e).  The other fields are those of instr_desc.
+__host__ __device__ constexpr uint32_t instr_desc_bs(uint32_t a_fmt, uint32_t b_fmt,
+                                                     uint32_t b_mn_major, uint32_t M, uint32_t N,
+                                                     uint32_t sfa_id, uint32_t sfb_id) {
+  return (sfb_id << 4) | (a_fmt << 7) | (b_fmt << 10) | (0u << 15) | (b_mn_major << 16) |
+         ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) | (sfa_id << 29);
+}
+
 // D[tmem] (+)= A[smem] * B[smem]
 template <int KIND_F8>
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -315,6 +327,35 @@ __device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, u
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
   }
+}
+
+// D[tmem] (+)= (A[tmem] x SFA) * (B[smem] x SFB), e4m3 operands, one UE8M0
+// scale per row of A (and per column of B) per 32-deep slice of K; the
+// scale factors are read from tensor memory at sfa_tmem / sfb_tmem.
+__device__ __forceinline__ void mma_ts_bs(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], [%1], %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Warp-collective form of mma_ts_bs (see mma_ss_elect).
+__device__ __forceinline__ void mma_ts_bs_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t sfa_tmem,
+                                                uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], [%1], %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
 }
 
 // Commit of everything the elected lane issued (see mma_ss_elect).
@@ -491,6 +532,11 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
       "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
       "r"(r[15])
       : "memory");
+}
+
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(r)
+               : "memory");
 }
 
 __device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t* r) {

@@ -149,9 +149,17 @@ ZYFA_API int zyfa_device_status(int* value, int reset);
  *       sum to one; the LSE as in 0.
  *     2: as 1, and the LSE is taken from that same rounded sum.
  *   Modes 1 and 2 add work to every tile of the softmax (slower).
+ *   ZYFA_OPT_BLOCK_SCALE (FP8 calls; BF16 calls ignore it): when 1, P is
+ *   scaled per row and 32-key slice by the power of two that brings the
+ *   slice's largest probability into the binade of p = 1 before it is
+ *   rounded to e4m3, and the P*V product is the block-scaled MMA, which
+ *   divides the same power of two back out (ZYFA README, "Kernel design":
+ *   per-block scaling, which keeps probabilities far below the row maximum
+ *   normal instead of subnormal or zero; GB300's scale blocks are 32 keys,
+ *   the page's 64).  Combines with ZYFA_OPT_ROUNDED_P.  Default 0; slower.
  * Returns ZYFA_OK or ZYFA_ERR_ARG.
  */
-enum { ZYFA_OPT_SERIALIZE_PV = 1, ZYFA_OPT_ROUNDED_P = 2 };
+enum { ZYFA_OPT_SERIALIZE_PV = 1, ZYFA_OPT_ROUNDED_P = 2, ZYFA_OPT_BLOCK_SCALE = 3 };
 ZYFA_API int zyfa_set_option(int option, int value);
 
 /*

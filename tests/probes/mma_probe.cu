@@ -5,7 +5,13 @@
 //                into 128-byte-swizzled K-major tiles (the S = Q K^T product);
 //   mode 1 (TS): D[128x128] = A[128x128] * B[128x128] with A written into
 //                tensor memory by tcgen05.st and B loaded by TMA as an MN-major
-//                operand (the O += P V product).
+//                operand (the O += P V product);
+//   mode 2/3 (TS, block-scaled, e4m3 only): as mode 1 with kind::mxf8f6f4 and
+//                one UE8M0 scale per row of A per 32-deep slice of K (B's
+//                scales all 2^0), the scale of row r and slice k written into
+//                tensor memory at lane r, byte k of one column (mode 2), or
+//                at lane 32q + r % 32 for every q, byte k of column r / 32
+//                (mode 3).
 //
 // f8 selects kind::f8f6f4 with e4m3 operands instead of kind::f16 with BF16.
 // One CTA of 128 threads; every wait is bounded.  A second probe lets a
@@ -27,14 +33,17 @@ template <int F8, int MODE>
 __global__ void __launch_bounds__(128, 1)
     mma_probe_kernel(const __grid_constant__ CUtensorMap tm_a,
                      const __grid_constant__ CUtensorMap tm_b, const uint8_t* a_glob,
-                     float* d_out) {
+                     const uint8_t* sf_glob, float* d_out) {
+  constexpr bool kBS = MODE >= 2;
+  static_assert(!kBS || F8, "block scaling is an e4m3 form");
   constexpr int kElem = F8 ? 1 : 2;
   constexpr int kChunkElems = 128 / kElem;     // elements per 128-byte row chunk
   constexpr int kChunks = 128 * kElem / 128;   // chunks per 128-element row
   constexpr int kChunkBytes = 128 * 128;       // 128 rows x 128 bytes
   constexpr int kUmmaK = 32 / kElem;
   constexpr uint32_t kFmt = F8 ? 0u : 1u;
-  constexpr uint32_t kIdesc = ptx::instr_desc(kFmt, kFmt, MODE == 1 ? 1u : 0u, 128, 128);
+  constexpr uint32_t kIdesc = ptx::instr_desc(kFmt, kFmt, MODE >= 1 ? 1u : 0u, 128, 128);
+  constexpr uint32_t kSfaCol = 192, kSfbCol = 224;   // scale factors of A and B
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -63,7 +72,8 @@ __global__ void __launch_bounds__(128, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  const uint32_t tmem = *tmem_slot;   // D at columns [0,128), A (TS) at [128, ...)
+  // D at columns [0,128), A (TS) at [128, ...), scale factors at 192 and 224.
+  const uint32_t tmem = *tmem_slot;
   bool ok = true;
 
   if (threadIdx.x == 0) {
@@ -78,7 +88,7 @@ __global__ void __launch_bounds__(128, 1)
     }
   }
   __syncwarp();
-  if (MODE == 1) {
+  if (MODE >= 1) {
     // Thread i writes row i of A (128 elements = 128*kElem bytes) into tensor
     // memory lane i, 4 bytes per column, in element order.
     const uint32_t* row = reinterpret_cast<const uint32_t*>(a_glob + threadIdx.x * 128 * kElem);
@@ -87,6 +97,33 @@ __global__ void __launch_bounds__(128, 1)
       uint32_t r[32];
       for (int i = 0; i < 32; ++i) r[i] = row[c + i];
       ptx::tmem_st32(tmem + lane_base + 128 + c, r);
+    }
+    if constexpr (kBS) {
+      const uint32_t ones[4] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu};
+      ptx::tmem_st4(tmem + lane_base + kSfbCol, ones);
+      auto word = [&](int r) {
+        const uint8_t* e = sf_glob + r * 4;
+        return uint32_t(e[0]) | (uint32_t(e[1]) << 8) | (uint32_t(e[2]) << 16) |
+               (uint32_t(e[3]) << 24);
+      };
+      if (MODE == 2) {
+        ptx::tmem_st1(tmem + lane_base + kSfaCol, word(threadIdx.x));
+      } else if (MODE == 3) {
+        const uint32_t w[4] = {word(lane), word(32 + lane), word(64 + lane), word(96 + lane)};
+        ptx::tmem_st4(tmem + lane_base + kSfaCol, w);
+      } else if (MODE == 4) {
+        // own quadrant only: lane r, column r / 32; zeros elsewhere
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        w[warp] = word(threadIdx.x);
+        ptx::tmem_st4(tmem + lane_base + kSfaCol, w);
+      } else {
+        // quadrant 0 only: lane r % 32, column r / 32; zeros elsewhere
+        uint32_t w[4] = {0u, 0u, 0u, 0u};
+        if (warp == 0) {
+          w[0] = word(lane); w[1] = word(32 + lane); w[2] = word(64 + lane); w[3] = word(96 + lane);
+        }
+        ptx::tmem_st4(tmem + lane_base + kSfaCol, w);
+      }
     }
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
@@ -106,6 +143,12 @@ __global__ void __launch_bounds__(128, 1)
           const uint32_t off = c * kChunkBytes + kk;
           ptx::mma_ss<F8>(tmem, ptx::smem_desc(a_addr + off, 16, 1024, 2u),
                           ptx::smem_desc(b_addr + off, 16, 1024, 2u), kIdesc, ks > 0);
+        } else if constexpr (kBS) {
+          // Slice ks takes byte ks of the scale-factor words.
+          const uint32_t idesc = ptx::instr_desc_bs(0u, 0u, 1u, 128, 128, ks, ks);
+          ptx::mma_ts_bs(tmem, tmem + 128 + ks * 8,
+                         ptx::smem_desc(b_addr + ks * kUmmaK * 128, kChunkBytes, 1024, 2u),
+                         idesc, tmem + kSfaCol, tmem + kSfbCol, ks > 0);
         } else {
           ptx::mma_ts<F8>(tmem, tmem + 128 + ks * 8,
                           ptx::smem_desc(b_addr + ks * kUmmaK * 128, kChunkBytes, 1024, 2u),
@@ -156,12 +199,13 @@ int make_map(EncodeTiledFn enc, CUtensorMap* m, const void* p, int f8) {
 
 template <int F8, int MODE>
 int run(const CUtensorMap& a, const CUtensorMap& b, const void* a_glob, float* d,
-        cudaStream_t s) {
+        cudaStream_t s, const void* sf = nullptr) {
   auto k = mma_probe_kernel<F8, MODE>;
   const int smem = 1024 + 2 * 2 * 128 * 128 + 256;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  k<<<1, 128, smem, s>>>(a, b, static_cast<const uint8_t*>(a_glob), d);
+  k<<<1, 128, smem, s>>>(a, b, static_cast<const uint8_t*>(a_glob),
+                         static_cast<const uint8_t*>(sf), d);
   return cudaGetLastError();
 }
 
@@ -225,6 +269,30 @@ __attribute__((visibility("default"))) int zyfa_probe_mma(int f8, int mode, cons
   if (f8 == 0 && mode == 1) return run<0, 1>(ma, mb, a, d, s);
   if (f8 == 1 && mode == 0) return run<1, 0>(ma, mb, a, d, s);
   if (f8 == 1 && mode == 1) return run<1, 1>(ma, mb, a, d, s);
+  return -1;
+}
+
+// Block-scaled form: a, b as mode 1 (e4m3 codes), sf: device 128 x 4 bytes,
+// the UE8M0 scale of row r of a and K slice k at sf[4 r + k]; layout 0
+// writes them as mode 2 of the probe kernel, layout 1 as mode 3.
+// d = (a x 2^(sf - 127)) * b.
+__attribute__((visibility("default"))) int zyfa_probe_mma_bs(int layout, const void* a, const void* b,
+                                                             const void* sf, float* d, void* stream) {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    return -5;
+  auto enc = reinterpret_cast<EncodeTiledFn>(fn);
+  CUtensorMap ma, mb;
+  if (make_map(enc, &ma, a, 1) != CUDA_SUCCESS || make_map(enc, &mb, b, 1) != CUDA_SUCCESS)
+    return -1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (layout == 0) return run<1, 2>(ma, mb, a, d, s, sf);
+  if (layout == 1) return run<1, 3>(ma, mb, a, d, s, sf);
+  if (layout == 2) return run<1, 4>(ma, mb, a, d, s, sf);
+  if (layout == 3) return run<1, 5>(ma, mb, a, d, s, sf);
   return -1;
 }
 
