@@ -1184,8 +1184,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // margin covers the rounding of exp2 and of the sum); otherwise
           // the warp forms the maximum and takes the tests exactly.
           const float bound = rs * 1.001f;
+          // (BF16 with the rounded-P denominator on every tile has no
+          // accuracy test: the denominator it would switch to is already
+          // the one in use; only the rescale test remains.)
           const bool quiet = C::kF8 ? (tacc & 0x80808080u) == 0u
-                                    : (bound <= C::kPCap && bound * C::kAccRatio <= l + rs);
+                                    : (bound <= C::kPCap &&
+                                       (C::kRoundedP || bound * C::kAccRatio <= l + rs));
           if (diag || !__all_sync(0xffffffffu, quiet)) {
           const float mx = row_max128(f) * c_log2;
           const bool need = mx > m_ref + C::kTau;
@@ -1216,7 +1220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A recomputed tile takes the rounded-sum denominator in the same
             // exp2 pass (right after a rescale its maximum carries most of
             // the mass the row has seen, so the test would pass anyway).
-            exact = any_need || __any_sync(0xffffffffu, p_max * 8.0f > l + rs);
+            exact = any_need ||
+                    (!C::kRoundedP && __any_sync(0xffffffffu, p_max * 8.0f > l + rs));
             if (exact) redo_bf16(f, c_log2, neg_m, t_s, any_need, rs, rr);
           }
           }
