@@ -354,14 +354,6 @@ __device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha) {
   }
 }
 
-// Sum of the four e4m3 values packed in w (exact FP16 values, added in
-// FP32 in byte order).
-__device__ __forceinline__ float e4m3x4_sum(uint32_t w) {
-  float d[4];
-  ptx::unpack_e4m3x4(w, d);
-  return (d[0] + d[1]) + (d[2] + d[3]);
-}
-
 // P for 64 scores (half h of the row): p = 2^(s*c + neg_m) by paired FMAs
 // and exp2, packed to BF16 (or e4m3; with two_term also the e4m3 rounding
 // residual at column offset 32), stored to tensor memory over S.  `sacc`
@@ -401,7 +393,7 @@ __device__ __forceinline__ void produce_half(const float* f, float c_log2, float
       if constexpr (C::kRoundedP) {
         float a2[2] = {0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) a2[i & 1] += e4m3x4_sum(pk[i]);
+        for (int i = 0; i < 8; ++i) a2[i & 1] = ptx::add_e4m3x4_f32(a2[i & 1], pk[i]);
         rr += a2[0] + a2[1];
       }
       if (two_term) {
@@ -417,7 +409,7 @@ __device__ __forceinline__ void produce_half(const float* f, float c_log2, float
         if constexpr (C::kRoundedP) {
           float a2[2] = {0.f, 0.f};
 #pragma unroll
-          for (int i = 0; i < 8; ++i) a2[i & 1] += e4m3x4_sum(lo[i]);
+          for (int i = 0; i < 8; ++i) a2[i & 1] = ptx::add_e4m3x4_f32(a2[i & 1], lo[i]);
           rr += a2[0] + a2[1];
         }
       }
@@ -484,8 +476,8 @@ __device__ __forceinline__ void redo_fp8(const float* f, float c_log2, float neg
     if constexpr (C::kRoundedP) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        if (do_hi) ra[i & 1] += e4m3x4_sum(hi[i]);
-        ra[i & 1] += e4m3x4_sum(lo[i]);
+        if (do_hi) ra[i & 1] = ptx::add_e4m3x4_f32(ra[i & 1], hi[i]);
+        ra[i & 1] = ptx::add_e4m3x4_f32(ra[i & 1], lo[i]);
       }
     }
   }
@@ -578,8 +570,8 @@ __device__ __forceinline__ void produce_bs(const float* f, float c_log2, float n
       float a2[2] = {0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        if constexpr (kHi) a2[i & 1] += e4m3x4_sum(hi[i]);
-        if constexpr (kLo) a2[i & 1] += e4m3x4_sum(lo[i]);
+        if constexpr (kHi) a2[i & 1] = ptx::add_e4m3x4_f32(a2[i & 1], hi[i]);
+        if constexpr (kLo) a2[i & 1] = ptx::add_e4m3x4_f32(a2[i & 1], lo[i]);
       }
       rr += (a2[0] + a2[1]) * down;
     }

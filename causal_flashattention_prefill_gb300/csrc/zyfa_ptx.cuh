@@ -630,6 +630,24 @@ __device__ __forceinline__ void add_e4m3x4_f16x2(uint32_t w, uint32_t& acc0, uin
       : "r"(w));
 }
 
+// acc plus the four e4m3 values packed in `w`: the codes are decoded to FP16
+// pairs (exact), byte 0 + byte 2 and byte 1 + byte 3 are added in FP16 (at
+// most one rounding each, relative 2^-11), and the two sums are added to acc
+// in FP32.
+__device__ __forceinline__ float add_e4m3x4_f32(float acc, uint32_t w) {
+  asm("{\n\t.reg .b16 lo, hi, s0, s1;\n\t.reg .b32 a, b, c;\n\t"
+      "mov.b32 {lo, hi}, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 a, lo;\n\t"
+      "cvt.rn.f16x2.e4m3x2 b, hi;\n\t"
+      "add.rn.f16x2 c, a, b;\n\t"
+      "mov.b32 {s0, s1}, c;\n\t"
+      "add.rn.f32.f16 %0, s0, %0;\n\t"
+      "add.rn.f32.f16 %0, s1, %0;\n\t}"
+      : "+f"(acc)
+      : "r"(w));
+  return acc;
+}
+
 // Exact FP32 values of the four e4m3 codes packed in `w` (byte 0 first).
 __device__ __forceinline__ void unpack_e4m3x4(uint32_t w, float (&d)[4]) {
   asm("{\n\t.reg .b16 lo, hi, h0, h1, h2, h3;\n\t.reg .b32 a, b;\n\t"
