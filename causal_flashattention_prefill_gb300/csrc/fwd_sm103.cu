@@ -156,6 +156,10 @@ struct Cfg {
   // measured faster; rolled, the FP8 and d_qk = 192 forms measured 5-12 %
   // faster on activation-like rows and short sequences.
   static constexpr bool kRollStages = kF8 || DQK == 192;
+  // BF16 d_qk = 128: the speculative pass keeps one sum per 32-key chunk,
+  // whose largest bounds the tile's p in the quiet test (about 4x tighter
+  // than the tile sum on flat rows; measured slower on the d_qk = 192 form).
+  static constexpr bool kChunkBound = !kF8 && DQK == 128;
   static_assert(kRollStages || (!kF8 && kSlotsFit >= 3),
                 "the unrolled stage loop carries neither the FP8 residual P V nor the piece ring");
   static constexpr int kOtherRegs = (!kF8 && DQK == 192) ? 136 : 104;
@@ -366,19 +370,25 @@ __device__ __forceinline__ void produce_half(const float* f, float c_log2, float
                                              uint32_t t_s, int h, bool two_term,
                                              float2 (&sacc)[2], float& rr, uint32_t tk = 0,
                                              uint32_t* tacc = nullptr, int cc0 = 0,
-                                             int ncc = 2) {
+                                             int ncc = 2, float* csum = nullptr) {
   const float2 c2 = make_float2(c_log2, c_log2);
   const float2 nm2 = make_float2(neg_m, neg_m);
 #pragma unroll
   for (int cc = cc0; cc < cc0 + ncc; ++cc) {
     const int ch = 2 * h + cc;  // 32-column chunk of the row
     float e[32];
+    float2 cacc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float2 (&acc)[2] = csum ? cacc : sacc;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const float2 x = __ffma2_rn(make_float2(f[32 * ch + 2 * i], f[32 * ch + 2 * i + 1]), c2, nm2);
       e[2 * i] = ptx::ex2(x.x);
       e[2 * i + 1] = ptx::ex2(x.y);
-      sacc[i & 1] = __fadd2_rn(sacc[i & 1], make_float2(e[2 * i], e[2 * i + 1]));
+      acc[i & 1] = __fadd2_rn(acc[i & 1], make_float2(e[2 * i], e[2 * i + 1]));
+    }
+    if (csum) {
+      const float2 t = __fadd2_rn(cacc[0], cacc[1]);
+      csum[ch] = t.x + t.y;
     }
     if constexpr (C::kF8) {
       uint32_t pk[8];
@@ -1083,8 +1093,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // normalised output.  BF16 then sums the denominator over the same
         // rounded values that multiply V (ZYFA README, "Accuracy"); FP8
         // keeps P as two e4m3 terms, hi + lo, lo being the rounding residual
-        // of hi (about 8 significant bits together; also on every diagonal
-        // tile, whose rows see few keys), and the MMA issuer adds a second
+        // of hi (about 8 significant bits together; always on a row's first
+        // tile), and the MMA issuer adds a second
         // P V product for lo when any warp of the stage flags the tile (the
         // other warps store zeros as their lo term).  On other tiles the
         // rounding errors average out and the unrounded sum stands in.
@@ -1164,25 +1174,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t acc_code = ptx::pack_e4m3x4(l * (1.0f / C::kAccRatio), 0.f, 0.f, 0.f) & 0xFFu;
             tk = threshold_addend(acc_code < cap_code ? acc_code : cap_code);
           }
-          produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 0, false, sacc, rr, tk, &tacc, 0, 1);
+          // BF16 d_qk = 128: per 32-key chunk sums, the largest of which
+          // bounds every p of the tile (the whole tile sum elsewhere).
+          float cs[4];
+          float* csp = C::kChunkBound ? cs : nullptr;
+          produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 0, false, sacc, rr, tk, &tacc, 0, 1, csp);
           wait_rest();
-          produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 0, false, sacc, rr, tk, &tacc, 1, 1);
-          produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 1, false, sacc, rr, tk, &tacc);
-          const float2 t2 = __fadd2_rn(sacc[0], sacc[1]);
-          rs = t2.x + t2.y;
+          produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 0, false, sacc, rr, tk, &tacc, 1, 1, csp);
+          produce_half<C, false, C::kF8>(f, c_log2, neg_m, t_s, 1, false, sacc, rr, tk, &tacc, 0, 2, csp);
+          if constexpr (!C::kChunkBound) {
+            const float2 t2 = __fadd2_rn(sacc[0], sacc[1]);
+            rs = t2.x + t2.y;
+          } else {
+            rs = (cs[0] + cs[1]) + (cs[2] + cs[3]);
+          }
           // The unrounded sum bounds every p of the tile (all p >= 0).  When
           // it is small enough, neither the rescale test nor the accuracy
           // test can fire and the tile maximum is not needed (the 0.1%
           // margin covers the rounding of exp2 and of the sum); otherwise
           // the warp forms the maximum and takes the tests exactly.
-          const float bound = rs * 1.001f;
+          const float bound =
+              (C::kChunkBound ? fmaxf(fmaxf(cs[0], cs[1]), fmaxf(cs[2], cs[3])) : rs) * 1.001f;
           // (BF16 with the rounded-P denominator on every tile has no
           // accuracy test: the denominator it would switch to is already
           // the one in use; only the rescale test remains.)
           const bool quiet = C::kF8 ? (tacc & 0x80808080u) == 0u
                                     : (bound <= C::kPCap &&
                                        (C::kRoundedP || bound * C::kAccRatio <= l + rs));
-          if (diag || !__all_sync(0xffffffffu, quiet)) {
+          if ((!C::kF8 && diag) || !__all_sync(0xffffffffu, quiet)) {
           const float mx = row_max128(f) * c_log2;
           const bool need = mx > m_ref + C::kTau;
           const bool any_need = __any_sync(0xffffffffu, need);
@@ -1206,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A recomputed tile takes the two-term P in the same exp2 pass
             // (right after a rescale its maximum carries most of the mass
             // the row has seen, so the test below would pass anyway).
-            two_term = any_need || diag || __any_sync(0xffffffffu, p_max * 32.0f > l + rs);
+            two_term = any_need || __any_sync(0xffffffffu, p_max * 32.0f > l + rs);
             if (two_term) redo_fp8<C>(f, c_log2, neg_m, t_s, any_need, rs, rr);
           } else {
             // A recomputed tile takes the rounded-sum denominator in the same
