@@ -346,7 +346,8 @@ __device__ __forceinline__ float pow2_neg(float e) {
   return __int_as_float((127 - static_cast<int>(e)) << 23);
 }
 
-// O of the row times alpha, in tensor memory.
+// O of the row times alpha, in tensor memory.  (The scores stay live
+// across a rescale, so O goes through 32 registers at a time.)
 __device__ __forceinline__ void rescale_o(uint32_t t_o, float alpha) {
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
@@ -1271,15 +1272,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.layout == 0
               ? ((static_cast<int64_t>(it.b) * p.S + row) * p.H + it.h) * kDV
               : ((static_cast<int64_t>(it.b) * p.H + it.h) * p.S + row) * kDV;
-#pragma unroll 1
+      // All of O in one tensor-memory load and wait (each load waits
+      // hundreds of cycles while the other stage's MMAs stream).
+      uint32_t o[128];
+      ptx::tmem_ld128_wait(t_o, o);
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        ptx::tmem_ld32_wait(t_o + c * 32, o);
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          pk[i] = ptx::pack_bf16x2(__uint_as_float(o[2 * i]) * inv,
-                                   __uint_as_float(o[2 * i + 1]) * inv);
+          pk[i] = ptx::pack_bf16x2(__uint_as_float(o[32 * c + 2 * i]) * inv,
+                                   __uint_as_float(o[32 * c + 2 * i + 1]) * inv);
         if (valid) {
           uint4* dst = reinterpret_cast<uint4*>(out + orow + c * 32);
 #pragma unroll
