@@ -138,8 +138,10 @@ struct Cfg {
   // Largest p that needs no rescale: 2^(tau + pre-scale).
   static constexpr float kPCap = exp2i(kTauBits + kPLog2Bits);
   // Accuracy test: a p above 1/kAccRatio of the row's mass so far takes the
-  // exact path (BF16 rounded-sum denominator, FP8 two-term P).
-  static constexpr float kAccRatio = kF8 ? 32.0f : 8.0f;
+  // exact path (BF16 rounded-sum denominator, FP8 two-term P).  FP8 with the
+  // rounded-P denominator keeps 1/32: its LSE mode sums the rounded values,
+  // whose error the two-term tiles bound.
+  static constexpr float kAccRatio = kF8 ? (kRoundedP ? 32.0f : 16.0f) : 8.0f;
   static constexpr uint32_t kFmt = kF8 ? 0u : 1u;   // E4M3 / BF16
   static constexpr uint32_t kIdescQK = ptx::instr_desc(kFmt, kFmt, 0, kBM, kBN);
   static constexpr uint32_t kIdescPV = ptx::instr_desc(kFmt, kFmt, 1, kBM, kDV);
@@ -1089,8 +1091,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c > row_in_tile) f[c] = -INFINITY;
         }
         // Accuracy of the rounded P (decided per warp from the tile's actual
-        // maximum): a probability that carries at least 1/8 (BF16) or 1/32
-        // (FP8) of the row's mass so far would show its rounding in the
+        // maximum): a probability that carries at least 1/8 (BF16) or 1/16
+        // (FP8; 1/32 with the rounded-P denominator) of the row's mass so far
+        // would show its rounding in the
         // normalised output.  BF16 then sums the denominator over the same
         // rounded values that multiply V (ZYFA README, "Accuracy"); FP8
         // keeps P as two e4m3 terms, hi + lo, lo being the rounding residual
@@ -1226,7 +1229,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // A recomputed tile takes the two-term P in the same exp2 pass
             // (right after a rescale its maximum carries most of the mass
             // the row has seen, so the test below would pass anyway).
-            two_term = any_need || __any_sync(0xffffffffu, p_max * 32.0f > l + rs);
+            two_term = any_need || __any_sync(0xffffffffu, p_max * C::kAccRatio > l + rs);
             if (two_term) redo_fp8<C>(f, c_log2, neg_m, t_s, any_need, rs, rr);
           } else {
             // A recomputed tile takes the rounded-sum denominator in the same
