@@ -222,13 +222,12 @@ struct Bars {
   static constexpr int kQFull = 0;            // [2]
   static constexpr int kQEmpty = 2;           // [2]
   static constexpr int kSFull = 4;            // [2]
-  static constexpr int kPFull = 6;            // [2]
-  static constexpr int kOFull = 8;            // [2]
-  static constexpr int kDrain = 10;
-  static constexpr int kPvDone = 11;          // [2]
-  static constexpr int kSlotFull = 13;        // [NS]
-  static constexpr int kSlotEmpty = 13 + NS;  // [NS]
-  static constexpr int kCount = 13 + 2 * NS;
+  static constexpr int kOFull = 6;            // [2]
+  static constexpr int kDrain = 8;
+  static constexpr int kPvDone = 9;           // [2]
+  static constexpr int kSlotFull = 11;        // [NS]
+  static constexpr int kSlotEmpty = 11 + NS;  // [NS]
+  static constexpr int kCount = 11 + 2 * NS;
 };
 
 // Placement of K/V tiles in the ring.  The producer and the MMA issuer walk
@@ -644,8 +643,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(B::kQEmpty + 1), 1);
     ptx::mbar_init(bar(B::kSFull + 0), 1);
     ptx::mbar_init(bar(B::kSFull + 1), 1);
-    ptx::mbar_init(bar(B::kPFull + 0), 4);
-    ptx::mbar_init(bar(B::kPFull + 1), 4);
     ptx::mbar_init(bar(B::kOFull + 0), 1);
     ptx::mbar_init(bar(B::kOFull + 1), 1);
     ptx::mbar_init(bar(B::kDrain), 1);
@@ -820,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The whole warp runs the issuing loop (every value in it is
     // warp-uniform) and one elected lane issues each MMA and commit.
     {
-      uint32_t q_par = 0, p_par = 0, pv_par = 0;  // bit s: phase parity per stage
+      uint32_t q_par = 0, pv_par = 0;  // bit s: phase parity per stage
       uint32_t p_count[2] = {0u, 0u};             // P tiles received per stage
       uint32_t t = 0;     // slot ring: K/V tiles consumed so far
       Ring<C> ring;       // chunk-piece ring: placement
@@ -952,9 +949,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto run_stage = [&](int s) -> bool {
               const int ns = s == 0 ? it.n0 : it.n1;
               if (j >= ns) return true;
-              ok = warp_wait(bar(B::kPFull + s), (p_par >> s) & 1u, abort, status, lane);
-              if (!ok) return false;
-              p_par ^= 1u << s;
+              // P of stage s: named barrier 1 + s with its four softmax warps.
+              ptx::bar_sync(1 + s, 160);
+              if (*abort) {
+                ok = false;
+                return false;
+              }
               const uint32_t pcount = s == 0 ? ++p_count[0] : ++p_count[1];
               ptx::tc_fence_after();
               // The flag is read before the MMAs are issued and used after
@@ -1002,9 +1002,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < 2; ++s) {
               const int ns = s == 0 ? it.n0 : it.n1;
               if (j >= ns) continue;
-              ok = warp_wait(bar(B::kPFull + s), (p_par >> s) & 1u, abort, status, lane);
-              if (!ok) break;
-              p_par ^= 1u << s;
+              ptx::bar_sync(1 + s, 160);
+              if (*abort) {
+                ok = false;
+                break;
+              }
               ++p_count[s];
               ptx::tc_fence_after();
               issue_pv(s, vb, j > 0, 0);
@@ -1255,10 +1257,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
         __syncwarp();
-        // P ready: the arrival goes through a tcgen05.commit of one lane (no
-        // MMA of this thread is outstanding, so it arrives at once); it woke
-        // the MMA issuer sooner than a thread's mbarrier.arrive (FP8 +1.6 %).
-        ptx::mma_commit_elect(bar(B::kPFull + s));
+        // P ready: the four softmax warps of the stage arrive on hardware
+        // barrier 1 + s, on which the MMA issuer warp waits (bar.sync).  A
+        // hardware barrier wakes the issuer sooner than an mbarrier phase
+        // (1-3 %).  It has no time limit, so its arrivals are guaranteed by
+        // construction: every wait a softmax warp passes before an arrival
+        // is bounded, a warp that gives up arrives once more on its way out
+        // (below), and the issuer reads the abort flag after every wait.
+        if (lane == 0) __threadfence_block();   // the pflag store before the arrival
+        __syncwarp();
+        ptx::bar_arrive(1 + s, 160);
       }
       if (!ok) break;
       // Epilogue: O * v_descale / lr as BF16 (FP8: the 2^4 pre-scale of P
@@ -1303,6 +1311,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::tc_fence_before();
     }
+    // A softmax warp that gives up releases an MMA issuer that may be waiting
+    // for its P (the issuer then sees the abort flag and unwinds).
+    if (!ok) ptx::bar_arrive(1 + s, 160);
   }
 
   // ---------------------------------------------------------------- teardown
