@@ -22,6 +22,7 @@ from ._lib import (  # noqa: F401
     ZYFA_FP8_E4M3,
     ZYFA_OK,
     ZYFA_OPT_BLOCK_SCALE,
+    ZYFA_OPT_DYNAMIC_SCHEDULE,
     ZYFA_OPT_ROUNDED_P,
     ZYFA_OPT_SERIALIZE_PV,
     load,

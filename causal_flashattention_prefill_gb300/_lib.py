@@ -29,6 +29,7 @@ ZYFA_BHSD = 1
 ZYFA_OPT_SERIALIZE_PV = 1
 ZYFA_OPT_ROUNDED_P = 2
 ZYFA_OPT_BLOCK_SCALE = 3
+ZYFA_OPT_DYNAMIC_SCHEDULE = 4
 
 # name -> (restype, argtypes); the C ABI of include/zyfa.h
 _P = ctypes.c_void_p

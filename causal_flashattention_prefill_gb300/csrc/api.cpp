@@ -25,6 +25,7 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
 std::atomic<int> g_serialize_pv{0};
 std::atomic<int> g_rounded_p{0};
 std::atomic<int> g_block_scale{0};
+std::atomic<int> g_dynamic_schedule{0};
 
 constexpr int kMaxDevices = 64;
 
@@ -258,8 +259,15 @@ int zyfa_fwd_scaled(const void* q, const void* k, const void* v, void* out, floa
   p.serialize_pv = g_serialize_pv.load(std::memory_order_relaxed);
   p.rounded_p = g_rounded_p.load(std::memory_order_relaxed);
   p.block_scale = g_block_scale.load(std::memory_order_relaxed);
+  p.dynamic_schedule = g_dynamic_schedule.load(std::memory_order_relaxed);
   p.softmax_scale = softmax_scale;
-  const int grid = p.total_items < sms ? p.total_items : sms;
+  // Static schedule: one persistent CTA per SM.  Dynamic: one CTA per item,
+  // of which about one per SM runs at a time and takes the items of the
+  // CTAs that have not started.
+  // (The dynamic schedule covers the default softmax modes; with the
+  // rounded-P or block-scaled options the static one is used.)
+  if (p.rounded_p != 0 || (dtype == ZYFA_FP8_E4M3 && p.block_scale != 0)) p.dynamic_schedule = 0;
+  const int grid = (p.dynamic_schedule || p.total_items < sms) ? p.total_items : sms;
   const int e = zyfa::launch_fwd(dtype, d_qk, p, maps, grid, device,
                                  reinterpret_cast<cudaStream_t>(stream));
   return e == 0 ? ZYFA_OK : ZYFA_ERR_LAUNCH;
@@ -311,6 +319,11 @@ int zyfa_set_option(int option, int value) {
   if (option == ZYFA_OPT_BLOCK_SCALE) {
     if (value < 0 || value > 1) return ZYFA_ERR_ARG;
     g_block_scale.store(value);
+    return ZYFA_OK;
+  }
+  if (option == ZYFA_OPT_DYNAMIC_SCHEDULE) {
+    if (value < 0 || value > 1) return ZYFA_ERR_ARG;
+    g_dynamic_schedule.store(value);
     return ZYFA_OK;
   }
   return ZYFA_ERR_ARG;

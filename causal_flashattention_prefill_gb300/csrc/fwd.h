@@ -23,6 +23,7 @@ struct FwdParams {
   int rounded_p;             // 0: default; 1: O's denominator from the rounded P on
                              // every tile; 2: that and the LSE from the same sum
   int block_scale;           // FP8: P scaled per 32-key slice, block-scaled P V
+  int dynamic_schedule;      // one CTA per item, items taken by cancelling CTAs
   float softmax_scale;
 };
 

@@ -183,16 +183,28 @@ struct Item {
   int nload;      // K/V tiles loaded = max(n0, n1)
 };
 
-// Work items are ordered longest first: query block u descending, then batch,
-// then head (so the query heads of one KV group run side by side and share
-// K/V in L2).  CTA c of G takes, in round r, item r*G + c for even r and
-// r*G + G-1-c for odd r (a serpentine deal that evens out the decreasing
-// costs).  Stage 0 (tile 2u) needs K/V tiles 0..2u; stage 1 (tile 2u+1)
-// needs 0..2u+1 and is idle when all its rows lie past the sequence end.
+// Items (numbered longest first, see decode_item) reach a CTA in one of two
+// ways.  Static (default): a grid of min(items, SMs) CTAs; CTA c of G takes,
+// in round r, item r*G + c for even r and r*G + G-1-c for odd r (a
+// serpentine deal that evens out the decreasing costs).  Dynamic
+// (ZYFA_OPT_DYNAMIC_SCHEDULE): one CTA per item; a running CTA takes the
+// items of CTAs that have not started by cancelling them (cluster launch
+// control), so the longest remaining item goes to whichever SM frees up
+// first -- better where item costs vary with the data, slightly worse on
+// regular rows; the producer warp makes the requests and passes the item
+// sequence to the MMA issuer and the softmax warps through a ring of
+// kItemRing slots (in the static schedule every warp computes it).
 __device__ __forceinline__ int item_index(int round, int cta, int grid) {
   return round * grid + ((round & 1) ? (grid - 1 - cta) : cta);
 }
 
+constexpr int kItemRing = 4;
+constexpr int kItemConsumers = 9;   // the MMA issuer warp and eight softmax warps
+
+// Item w, the w-th longest: query block u descending, then batch, then head
+// (so the query heads of one KV group run side by side and share K/V in
+// L2).  Stage 0 (tile 2u) needs K/V tiles 0..2u; stage 1 (tile 2u+1) needs
+// 0..2u+1 and is idle when all its rows lie past the sequence end.
 __device__ __forceinline__ Item decode_item(int w, const FwdParams& p) {
   Item it;
   const int per_block = p.B * p.H;
@@ -214,6 +226,8 @@ struct Smem {
   uint32_t* tmem_base;
   int* abort;
   volatile uint32_t* pflag;   // [stage]: index of the last tile with a two-term FP8 P
+  volatile int* items;        // [kItemRing]: item sequence (-1: no more items)
+  uint32_t clc_resp;          // shared-memory address of the 16-byte cancel response
 };
 
 // Barrier indices inside the barrier array.
@@ -225,9 +239,12 @@ struct Bars {
   static constexpr int kOFull = 6;            // [2]
   static constexpr int kDrain = 8;
   static constexpr int kPvDone = 9;           // [2]
-  static constexpr int kSlotFull = 11;        // [NS]
-  static constexpr int kSlotEmpty = 11 + NS;  // [NS]
-  static constexpr int kCount = 11 + 2 * NS;
+  static constexpr int kItemFull = 11;        // [kItemRing]
+  static constexpr int kItemEmpty = 15;       // [kItemRing]
+  static constexpr int kClc = 19;             // cancel response landed
+  static constexpr int kSlotFull = 20;        // [NS]
+  static constexpr int kSlotEmpty = 20 + NS;  // [NS]
+  static constexpr int kCount = 20 + 2 * NS;
 };
 
 // Placement of K/V tiles in the ring.  The producer and the MMA issuer walk
@@ -607,12 +624,13 @@ __device__ __forceinline__ void produce_tile(const float* f, float c_log2, float
 
 }  // namespace
 
-template <int DT, int DQK, int RP, int BS>
+template <int DT, int DQK, int RP, int BS, int DS>
 __global__ void __launch_bounds__(kThreads, 1)
     zyfa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = Cfg<DT, DQK, RP, BS>;
+  constexpr bool kDynamic = DS != 0;   // dynamic schedule (see item_index)
   constexpr int NS = C::kNumPieces;
   using B = Bars<NS>;
 
@@ -627,6 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   sm.tmem_base = reinterpret_cast<uint32_t*>(sm.bars + B::kCount);
   sm.abort = reinterpret_cast<int*>(sm.tmem_base + 1);
   sm.pflag = reinterpret_cast<volatile uint32_t*>(sm.abort + 1);
+  sm.items = reinterpret_cast<volatile int*>(sm.pflag + 2);
+  sm.clc_resp = (ptx::smem_u32(const_cast<int*>(sm.items) + kItemRing) + 15u) & ~15u;
   volatile int* abort = sm.abort;
 
   const int warp = threadIdx.x >> 5;
@@ -648,6 +668,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::mbar_init(bar(B::kDrain), 1);
     ptx::mbar_init(bar(B::kPvDone + 0), 1);
     ptx::mbar_init(bar(B::kPvDone + 1), 1);
+    for (int i = 0; i < kItemRing; ++i) {
+      ptx::mbar_init(bar(B::kItemFull + i), 1);
+      ptx::mbar_init(bar(B::kItemEmpty + i), kItemConsumers);
+    }
+    ptx::mbar_init(bar(B::kClc), 1);
     for (int i = 0; i < NS; ++i) {
       ptx::mbar_init(bar(B::kSlotFull + i), 1);
       ptx::mbar_init(bar(B::kSlotEmpty + i), 1);
@@ -674,8 +699,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *sm.tmem_base;
 
   int* status = &g_zyfa_status;
-  const int grid = gridDim.x;
-  const int cta = blockIdx.x;
+  // Item r of this CTA's sequence for a consuming warp (the MMA issuer or a
+  // softmax warp), -1 after the last: computed in the static schedule; in
+  // the dynamic one, read from the producer's slot, which is then released.
+  auto take_item = [&](int r, int& w) -> bool {
+    if constexpr (!kDynamic) {
+      w = item_index(r, blockIdx.x, gridDim.x);
+      if (w >= p.total_items) w = -1;
+      return true;
+    } else {
+      const int slot = r & (kItemRing - 1);
+      if (!warp_wait(bar(B::kItemFull + slot), static_cast<uint32_t>(r / kItemRing) & 1u, abort,
+                     status, lane))
+        return false;
+      w = sm.items[slot];
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(B::kItemEmpty + slot));
+      return true;
+    }
+  };
 
   // Each setmaxnreg sits inside its role's branch so that the register
   // allocator sees the softmax code only on the 224-register path.
@@ -707,9 +749,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t own_b = 0, own_par = 0, own_valid = 0, rel_par = 0;
       const int group = p.H / p.Hkv;
       bool ok = true;
+      int w = blockIdx.x;       // this CTA's own item first
+      bool more = true;
+      uint32_t clc_par = 0;
+      bool clc_pending = false;
       for (int r = 0; ok; ++r) {
-        const int w = item_index(r, cta, grid);
-        if (w >= p.total_items) break;
+        if constexpr (kDynamic) {
+          // Item r (or the end) to the MMA issuer and the softmax warps.
+          const int islot = r & (kItemRing - 1);
+          if (r >= kItemRing) {
+            ok = ptx::mbar_wait(bar(B::kItemEmpty + islot),
+                                (static_cast<uint32_t>(r / kItemRing) & 1u) ^ 1u, abort, status,
+                                1);
+            if (!ok) break;
+          }
+          sm.items[islot] = more ? w : -1;
+          ptx::mbar_arrive(bar(B::kItemFull + islot));
+        }
+        if (!more) break;
         const Item it = decode_item(w, p);
         const int nst = it.n1 > 0 ? 2 : 1;
         for (int s = 0; s < nst && ok; ++s) {
@@ -800,8 +857,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (!ok) break;
+        if constexpr (kDynamic) {
+          // The next item: a CTA of this grid that has not started, if any.
+          ptx::mbar_arrive_expect_tx(bar(B::kClc), 16);
+          ptx::clc_try_cancel(sm.clc_resp, bar(B::kClc));
+          clc_pending = true;
+          ok = ptx::mbar_wait(bar(B::kClc), clc_par, abort, status, 1);
+          if (!ok) break;
+          clc_pending = false;
+          clc_par ^= 1u;
+          int x = 0;
+          more = ptx::clc_query(sm.clc_resp, x);
+          w = x;
+        } else {
+          w = item_index(r + 1, blockIdx.x, gridDim.x);
+          more = w < p.total_items;
+        }
       }
       if (!ok) {
+        if (clc_pending) ptx::mbar_drain(bar(B::kClc), clc_par);
         // Unwind: let every copy this thread issued land before the CTA's
         // shared memory is released (each copy completes on the last
         // arming of some full barrier).
@@ -884,8 +959,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
 
       for (int r = 0; ok; ++r) {
-        const int w = item_index(r, cta, grid);
-        if (w >= p.total_items) break;
+        int w = -1;
+        ok = take_item(r, w);
+        if (!ok || w < 0) break;
         const Item it = decode_item(w, p);
         const int nst = it.n1 > 0 ? 2 : 1;
         for (int s = 0; s < nst && ok; ++s) {
@@ -1055,8 +1131,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t s_uses = 0, o_uses = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int w = item_index(r, cta, grid);
-      if (w >= p.total_items) break;
+      int w = -1;
+      ok = take_item(r, w);
+      if (!ok || w < 0) break;
       const Item it = decode_item(w, p);
       const int ns = s == 0 ? it.n0 : it.n1;
       if (ns == 0) continue;
@@ -1328,12 +1405,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The dynamic shared-memory limit is raised once per device and
 // instantiation.  Should a launch still be refused (the attribute is lost
 // when a device is reset), it is raised again and the launch retried once.
-template <int DT, int DQK, int RP, int BS = 0>
+template <int DT, int DQK, int RP, int BS = 0, int DS = 0>
 static int launch_one(const FwdParams& p, const TensorMaps& m, int grid, int device,
                       cudaStream_t stream) {
   using C = Cfg<DT, DQK, RP, BS>;
   static std::atomic<uint64_t> attr_set{0};   // bit d: raised on device d
-  auto kern = zyfa_fwd_kernel<DT, DQK, RP, BS>;
+  auto kern = zyfa_fwd_kernel<DT, DQK, RP, BS, DS>;
   const uint64_t bit = 1ull << device;
   auto raise_limit = [&]() -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1358,6 +1435,15 @@ static int launch_one(const FwdParams& p, const TensorMaps& m, int grid, int dev
 int launch_fwd(int dtype, int d_qk, const FwdParams& p, const TensorMaps& maps, int grid,
                int device, cudaStream_t stream) {
   if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+  if (p.dynamic_schedule) {
+    // Dynamic schedule: the default softmax modes only (the host sizes the
+    // grid for the schedule it asks for, see api.cpp).
+    if (dtype == 0 && d_qk == 128) return launch_one<0, 128, 0, 0, 1>(p, maps, grid, device, stream);
+    if (dtype == 0 && d_qk == 192) return launch_one<0, 192, 0, 0, 1>(p, maps, grid, device, stream);
+    if (dtype == 1 && d_qk == 128) return launch_one<1, 128, 0, 0, 1>(p, maps, grid, device, stream);
+    if (dtype == 1 && d_qk == 192) return launch_one<1, 192, 0, 0, 1>(p, maps, grid, device, stream);
+    return cudaErrorInvalidValue;
+  }
   if (dtype == 1 && p.block_scale) {
     if (p.rounded_p == 0) {
       if (d_qk == 128) return launch_one<1, 128, 0, 1>(p, maps, grid, device, stream);

@@ -134,6 +134,38 @@ __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Cluster launch control (dynamic scheduling of a persistent grid): asks
+// the hardware to cancel a CTA of this grid that has not started yet.  The
+// 16-byte response lands at `resp` (shared memory, 16-byte aligned) and
+// completes `bar` with 16 transaction bytes.  After a response that reports
+// no cancellation, no further request may be made.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+      "[%0], [%1];" ::"r"(resp),
+      "r"(bar)
+      : "memory");
+}
+
+// Reads a response of clc_try_cancel: true, with the x index of the
+// cancelled CTA, when a CTA was cancelled (its work now belongs to the
+// caller); false when none was left.
+__device__ __forceinline__ bool clc_query(uint32_t resp, int& x) {
+  uint32_t ok, cx;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "mov.u32 %0, 0;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %1, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %0, r;\n\t}"
+      : "=r"(cx), "=r"(ok)
+      : "r"(resp)
+      : "memory");
+  x = static_cast<int>(cx);
+  return ok != 0;
+}
+
 // 2-D tiled load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                             int c0, int c1, uint64_t policy) {

@@ -157,9 +157,23 @@ ZYFA_API int zyfa_device_status(int* value, int reset);
  *   per-block scaling, which keeps probabilities far below the row maximum
  *   normal instead of subnormal or zero; GB300's scale blocks are 32 keys,
  *   the page's 64).  Combines with ZYFA_OPT_ROUNDED_P.  Default 0; slower.
+ *   ZYFA_OPT_DYNAMIC_SCHEDULE: when 1, work items (query blocks of 256 rows
+ *   of one head) go to whichever SM frees up first, longest first, instead
+ *   of the static deal over one persistent CTA per SM (ZYFA README, "Kernel
+ *   design": longest-first work distribution).  The outputs are the same
+ *   bits either way; dynamic helps when the cost of an item varies with the
+ *   data (rows whose maximum keeps rising), static is slightly faster on
+ *   regular rows.  It applies to the default softmax modes: with
+ *   ZYFA_OPT_ROUNDED_P or (FP8) ZYFA_OPT_BLOCK_SCALE set, the static
+ *   schedule is used.  Default 0.
  * Returns ZYFA_OK or ZYFA_ERR_ARG.
  */
-enum { ZYFA_OPT_SERIALIZE_PV = 1, ZYFA_OPT_ROUNDED_P = 2, ZYFA_OPT_BLOCK_SCALE = 3 };
+enum {
+  ZYFA_OPT_SERIALIZE_PV = 1,
+  ZYFA_OPT_ROUNDED_P = 2,
+  ZYFA_OPT_BLOCK_SCALE = 3,
+  ZYFA_OPT_DYNAMIC_SCHEDULE = 4
+};
 ZYFA_API int zyfa_set_option(int option, int value);
 
 /*

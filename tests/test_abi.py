@@ -42,7 +42,8 @@ def test_header_enums_match_binding():
     for name in ("ZYFA_OK", "ZYFA_ERR_ARG", "ZYFA_ERR_UNSUPPORTED", "ZYFA_ERR_ALIGN",
                  "ZYFA_ERR_LAUNCH", "ZYFA_ERR_DEVICE", "ZYFA_ERR_DEVICE_TIMEOUT", "ZYFA_BF16",
                  "ZYFA_FP8_E4M3", "ZYFA_BSHD", "ZYFA_BHSD", "ZYFA_OPT_SERIALIZE_PV",
-                 "ZYFA_OPT_ROUNDED_P", "ZYFA_OPT_BLOCK_SCALE"):
+                 "ZYFA_OPT_ROUNDED_P", "ZYFA_OPT_BLOCK_SCALE",
+                 "ZYFA_OPT_DYNAMIC_SCHEDULE"):
         m = re.search(rf"\b{name}\s*=\s*(-?\d+)", text)
         assert m, name
         assert int(m.group(1)) == getattr(zf, name), name
@@ -135,6 +136,9 @@ def test_options(lib):
         assert zf.zyfa_set_option(zf.ZYFA_OPT_BLOCK_SCALE, v) == zf.ZYFA_OK
     assert zf.zyfa_set_option(zf.ZYFA_OPT_BLOCK_SCALE, 2) == zf.ZYFA_ERR_ARG
     assert zf.zyfa_set_option(zf.ZYFA_OPT_BLOCK_SCALE, -1) == zf.ZYFA_ERR_ARG
+    for v in (1, 0):
+        assert zf.zyfa_set_option(zf.ZYFA_OPT_DYNAMIC_SCHEDULE, v) == zf.ZYFA_OK
+    assert zf.zyfa_set_option(zf.ZYFA_OPT_DYNAMIC_SCHEDULE, 2) == zf.ZYFA_ERR_ARG
     assert zf.zyfa_set_option(99, 1) == zf.ZYFA_ERR_ARG
 
 
