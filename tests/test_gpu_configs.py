@@ -32,7 +32,7 @@ FULL = [
      for S in (2048, 4096, 16384, 30000, 32768)]
 
 
-# The spec shapes (the S = 16384 GQA workloads and both MLA forms) are
+# The headline shapes (the S = 16384 GQA workloads and both MLA forms) are
 # checked on every head; the two-batch MHA sweep, whose oracle would cost
 # minutes per workload on all heads, on three heads per batch.
 ALL_HEADS = {"fp8_gqa_b1_h32kv8_s16384_d128", "bf16_gqa_b1_h32kv8_s16384_d128",
