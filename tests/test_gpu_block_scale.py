@@ -8,7 +8,7 @@ unscaled e4m3 values turn subnormal or zero).
 Parity with the float64 oracle under the FP8 tolerances, alone and with the
 rounded-P modes; bitwise determinism; and a row structure where the scaling
 decides the result: every key but the first lies about 14 binades below the
-first, so the unscaled P of those keys (times the 2^4 pre-scale) falls below
+first, so the unscaled P of those keys (times the kernel's pre-scale) falls below
 half the smallest e4m3 subnormal and rounds to zero, while the scaled P keeps
 three significant bits."""
 
