@@ -6,8 +6,10 @@
 // seqlen_k, MHA/GQA/MQA, d_qk = d_v = 128 or d_qk = 192 with d_v = 128,
 // BF16 or FP8 e4m3 inputs with one descale per tensor, BF16 output).
 //
-// One CTA per SM, persistent.  A work item is one query block of 256 rows
-// (two 128-row tiles, "stage 0" and "stage 1") of one (batch, head).  Both
+// One CTA per SM, persistent (or, with the dynamic schedule, one CTA per
+// work item, of which about one per SM runs and takes the items of CTAs that
+// have not started).  A work item is one query block of 256 rows (two
+// 128-row tiles, "stage 0" and "stage 1") of one (batch, head).  Both
 // tiles share every K/V tile that the CTA streams, so each K/V byte brought
 // on chip serves 256 query rows (the wider-query-tile idea of the CDNA4 post,
 // section 4.2, realised here as two tensor-memory accumulators).
@@ -18,7 +20,8 @@
 //   warp  8    TMA producer: Q tiles and a ring of K/V tiles (whole-tile
 //              slots, or 16 KB pieces for BF16 d_qk = 192)
 //   warp  9    MMA issuer: S = Q K^T (SS form) and O += P V (TS form, P read
-//              from tensor memory, V as an MN-major operand)
+//              from tensor memory, V as an MN-major operand); it learns that
+//              a stage's P is ready on hardware barrier 1 + stage
 //   warps 10-11 idle (they complete the third warpgroup so that registers
 //              can move to the softmax warpgroups with setmaxnreg)
 //
