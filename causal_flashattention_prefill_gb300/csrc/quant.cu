@@ -707,8 +707,6 @@ int read_rot_status(int* value, int reset) {
 // instead.  Every device that loads this library keeps these 4 KB until the
 // process exits, and every call on a device shares them.
 // ---------------------------------------------------------------------------
-#include <mutex>
-
 namespace zyfa {
 namespace {
 
@@ -719,36 +717,20 @@ static __device__ __align__(256) float g_noalloc_partials[kQuantMaxPartials];
 static_assert(sizeof(g_noalloc_partials) / sizeof(float) >= kQuantMaxPartials,
               "the array holds one maximum per CTA of the largest first pass");
 
-constexpr int kMaxDevicesNoAlloc = 64;
-std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[kMaxDevicesNoAlloc] = {};
-
 }  // namespace
 
 int fp8_quantize_noalloc(const void* x, int64_t n, int x_type, void* x8, float* descale, int sms,
                          cudaStream_t stream) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  // The array's device address is looked up on every call (a table lookup
+  // once the module is loaded): a cached address would go stale when a
+  // device reset reloads the module in a new context.
+  void* partials = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&partials, g_noalloc_partials);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevicesNoAlloc) return cudaErrorInvalidDevice;
-  float* partials = nullptr;
-  {
-    // One-time set-up per device, with that device current: host code needs
-    // the array's device address (its name is only a host-side stand-in).
-    // The address is kept for the life of the process, so the entry point is
-    // not usable on a device after cudaDeviceReset there.
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-      void* p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_noalloc_partials);
-      if (e != cudaSuccess) return e;
-      g_noalloc_ptr[dev] = static_cast<float*>(p);
-    }
-    partials = g_noalloc_ptr[dev];
-  }
   // Nothing needs clearing: the second pass reads only the slots the first
   // pass of the same call has written.
-  return launch_fp8_quantize(x, n, x_type, x8, descale, partials, sms, stream);
+  return launch_fp8_quantize(x, n, x_type, x8, descale, static_cast<float*>(partials), sms,
+                             stream);
 }
 
 }  // namespace zyfa
