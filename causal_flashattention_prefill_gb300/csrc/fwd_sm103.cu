@@ -1035,20 +1035,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (j >= ns) return true;
               // P of stage s: named barrier 1 + s with its four softmax warps.
               ptx::bar_sync(1 + s, 160);
-              if (*abort) {
+              // The abort flag and the lo-term flag are loaded here and used
+              // only once the P V MMAs are issued: a shared-memory load from
+              // this thread takes hundreds of cycles while the tensor core
+              // streams its operands, and the MMA queue would run dry if the
+              // issue waited for it.  (Should a softmax warp have given up,
+              // the P V MMAs read a P that nobody wrote: every operand is in
+              // range, and the launch's results are void anyway.)
+              const int abort_raw = *abort;
+              uint32_t lo_raw = 0;
+              if constexpr (C::kF8) lo_raw = sm.pflag[s];
+              const uint32_t pcount = s == 0 ? ++p_count[0] : ++p_count[1];
+              ptx::tc_fence_after();
+              issue_pv(s, vb, j > 0, 0);
+              if (C::kF8 && __shfl_sync(0xffffffffu, lo_raw, 0) == pcount)
+                issue_pv(s, vb, true, 32);  // lo term
+              if (__shfl_sync(0xffffffffu, abort_raw, 0)) {
                 ok = false;
                 return false;
               }
-              const uint32_t pcount = s == 0 ? ++p_count[0] : ++p_count[1];
-              ptx::tc_fence_after();
-              // The flag is read before the MMAs are issued and used after
-              // them: a shared-memory load from this thread takes hundreds of
-              // cycles while the tensor core streams its operands, and the
-              // MMA queue would run dry if the issue waited for it.
-              uint32_t lo_flag = 0;
-              if constexpr (C::kF8) lo_flag = __shfl_sync(0xffffffffu, sm.pflag[s], 0);
-              issue_pv(s, vb, j > 0, 0);
-              if (C::kF8 && lo_flag == pcount) issue_pv(s, vb, true, 32);  // lo term
               if constexpr (C::kChunkPieces) {
                 if (s == s_last_v) ptx::mma_commit_elect(bar(B::kSlotEmpty + slot_v));
               }
@@ -1087,13 +1092,14 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int ns = s == 0 ? it.n0 : it.n1;
               if (j >= ns) continue;
               ptx::bar_sync(1 + s, 160);
-              if (*abort) {
-                ok = false;
-                break;
-              }
+              const int abort_raw = *abort;   // used after the P V MMAs (as above)
               ++p_count[s];
               ptx::tc_fence_after();
               issue_pv(s, vb, j > 0, 0);
+              if (__shfl_sync(0xffffffffu, abort_raw, 0)) {
+                ok = false;
+                break;
+              }
               if (p.serialize_pv && j + 1 < ns) {
                 ptx::mma_commit_elect(bar(B::kPvDone + s));
                 ok = warp_wait(bar(B::kPvDone + s), (pv_par >> s) & 1u, abort, status, lane);
@@ -1348,8 +1354,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // (1-3 %).  It has no time limit, so its arrivals are guaranteed by
         // construction: every wait a softmax warp passes before an arrival
         // is bounded, a warp that gives up arrives once more on its way out
-        // (below), and the issuer reads the abort flag after every wait.
-        if (lane == 0) __threadfence_block();   // the pflag store before the arrival
+        // (below), and the issuer reads the abort flag after every wait
+        // (testing it once that stage's P V MMAs are issued).  Lane 0's
+        // lo-term flag store, on two-term FP8 tiles only, is fenced before
+        // the arrival; other tiles store nothing the issuer reads.
+        if (C::kF8 && two_term && lane == 0) __threadfence_block();
         __syncwarp();
         ptx::bar_arrive(1 + s, 160);
       }
