@@ -1240,12 +1240,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tmem_st4(t_s + kSfbCol, unit);
           if (j == 0 || diag || any_need) {
             two_term = true;
+            if (lane == 0) sm.pflag[s] = s_uses;
             produce_bs<C, true, true>(f, c_log2, neg_m, ex, t_s, rs, rr);
           } else {
             produce_bs<C, true, false>(f, c_log2, neg_m, ex, t_s, rs, rr);
             const float p_max = ptx::ex2(mx + neg_m);
             two_term = __any_sync(0xffffffffu, p_max * C::kAccRatio > l + rs);
-            if (two_term) produce_bs<C, false, true>(f, c_log2, neg_m, ex, t_s, rs, rr);
+            if (two_term) {
+              if (lane == 0) sm.pflag[s] = s_uses;
+              produce_bs<C, false, true>(f, c_log2, neg_m, ex, t_s, rs, rr);
+            }
           }
         } else if (j == 0) {
           // First tile of the row: the reference is this tile's maximum.
@@ -1253,6 +1257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_ref = row_max128(f) * c_log2;
           exact = !C::kF8;
           two_term = C::kF8;
+          if (C::kF8 && lane == 0) sm.pflag[s] = s_uses;
           produce_tile<C, !C::kF8>(f, c_log2, C::kPLog2Scale - m_ref, t_s, two_term, rs, rr);
         } else {
           // Exp2 against the current reference while the tile maximum is
@@ -1323,7 +1328,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // (right after a rescale its maximum carries most of the mass
             // the row has seen, so the test below would pass anyway).
             two_term = any_need || __any_sync(0xffffffffu, p_max * C::kAccRatio > l + rs);
-            if (two_term) redo_fp8<C>(f, c_log2, neg_m, t_s, any_need, rs, rr);
+            if (two_term) {
+              if (lane == 0) sm.pflag[s] = s_uses;
+              redo_fp8<C>(f, c_log2, neg_m, t_s, any_need, rs, rr);
+            }
           } else {
             // A recomputed tile takes the rounded-sum denominator in the same
             // exp2 pass (right after a rescale its maximum carries most of
@@ -1334,14 +1342,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           }
         }
-        if (C::kF8) {
-          if (two_term) {
-            if (lane == 0) sm.pflag[s] = s_uses;
-          } else {
-            const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        // FP8: a two-term tile's lane 0 has stored the tile's count as the
+        // lo-term flag as soon as the decision was taken (the store then
+        // completes during the lo pass, not at the fence below); other tiles
+        // store zeros as their lo term.  The MMA issuer reads the flag of
+        // this tile only after the arrival below, and its read of the
+        // previous tile's flag returned before it issued this tile's S, so
+        // the early store overwrites nothing it still needs.
+        if (C::kF8 && !two_term) {
+          const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll
-            for (int c = 0; c < 4; ++c) ptx::tmem_st8(t_s + 32 + c * 8, z);
-          }
+          for (int c = 0; c < 4; ++c) ptx::tmem_st8(t_s + 32 + c * 8, z);
         }
         l += rs;
         lr += (exact || C::kRoundedP) ? rr : rs;
